@@ -1,0 +1,463 @@
+"""Benchmark of the GB300 fused Compressor (forward + backward step).
+
+One step = csa_compress_fwd + csa_compress_bwd (forward kernel, backward
+kernel, dape reduce) over the 256k-token headline workload: ratio 4, coff 2,
+head_dim 512, 262144 tokens in 64 segments, capacity = true rows + 1024.
+Inputs are seeded synthetic data (workloads.config("headline")) resident in
+HBM; kv + score alone are 1 GiB, far above the 129 MB L2, so no flush is
+needed between steps.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on
+the host cores instead (the reference arm of this repository).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Compressor fwd/bwd tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+WORKLOAD = ("headline: ratio=4 coff=2 head_dim=512, 262144 tokens in 64 segments "
+            "(lengths U{1..8191} renormalised), capacity = true rows + 1024 padding rows")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=262144,
+                    help="scale the headline recipe to this many tokens (profiling runs)")
+    return ap.parse_args()
+
+
+def headline_case(tokens: int, seed: int, fill: bool = True):
+    """The headline workload, or the same recipe scaled to `tokens` tokens."""
+    import workloads
+    if tokens == 262144:
+        return workloads.config("headline", seed=seed, fill=fill)
+    nseg = max(1, round(64 * tokens / 262144))
+    lens = workloads.headline_seqlens(seed, total=tokens, nseg=nseg)
+    return workloads.make_case(f"headline@{tokens}", lens, 4, 2, 512,
+                               pad_rows=max(1, round(1024 * tokens / 262144)), seed=seed, fill=fill)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ bytes
+
+
+def algorithmic_bytes(case):
+    """Compulsory HBM bytes of one forward and one backward call, per the
+    scope table's per-token accounting: every (token, column) element of kv
+    and score read once; out written for every capacity row; the backward
+    also reads grad_out of the true rows and writes dkv / dscore in full;
+    ape read (and dape written) once."""
+    T, d, r, coff, C = case.total_tokens, case.head_dim, case.ratio, case.coff, case.capacity
+    R = case.true_rows
+    ape = r * coff * d * 4
+    fwd = T * coff * d * 2 * 2 + C * d * 2 + ape
+    bwd = 2 * T * coff * d * 2 * 2 + R * d * 2 + 2 * ape
+    return fwd, bwd
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_softmax_kv_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, units: float):
+    """DRAM bytes per launch of `kernel_key` from the committed ncu summary, scaled
+    to this launch's units; None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel_key]
+        if rec["source_hash"] != source_hash(rec["sources"]):
+            return None
+        return rec["dram_bytes_per_unit"] * units
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_rate(case, budget_s: float = 12.0, min_tokens: int = 16384):
+    """Tokens/s of the CPU oracle (fp32 fwd + bwd, all host cores) on a prefix
+    of the workload's segments sized from a short calibration run."""
+    import numpy as np
+    import oracle
+    import workloads
+
+    oracle.build()
+    cores = os.cpu_count() or 1
+
+    def sub_case(tokens):
+        lens, acc = [], 0
+        for L in case.seqlens:
+            take = int(min(L, tokens - acc))
+            if take <= 0:
+                break
+            lens.append(take)
+            acc += take
+        pad = max(0, round(1024 * acc / case.total_tokens))
+        return workloads.make_case("sample", lens, case.ratio, case.coff, case.head_dim,
+                                   pad_rows=pad, seed=1)
+
+    def run(c):
+        p = oracle.Problem(c.cu_seqlens, c.cu_seqlens_comp, c.total_tokens, c.capacity,
+                           c.ratio, c.coff, c.head_dim)
+        t0 = time.perf_counter()
+        oracle.fwd32(p, c.kv, c.score, c.ape, nthreads=cores)
+        oracle.bwd32(p, c.kv, c.score, c.ape, c.grad_out, nthreads=cores)
+        return time.perf_counter() - t0
+
+    cal = sub_case(min_tokens)
+    t_cal = run(cal)
+    per_token = t_cal / cal.total_tokens
+    tokens = int(min(case.total_tokens, max(min_tokens, budget_s / per_token)))
+    sample = sub_case(tokens)
+    t = run(sample)
+    return sample.total_tokens / t, cores, (
+        f"first {len(sample.seqlens)} segments of the workload ({sample.total_tokens} tokens, "
+        f"{sample.capacity} rows incl. proportional padding), O32 fwd + bwd once, {t:.1f} s"), sample
+
+
+# ------------------------------------------------------------------ arms
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+
+    case = headline_case(args.tokens, seed=0, fill=False)
+    steps, warm = args.steps, args.warmup
+    oracle.build()
+    cores = os.cpu_count() or 1
+    # one calibration, then a per-step sample sized so that the whole run ends in ~2 minutes
+    cal = workloads.make_case("cal", case.seqlens[:1], 4, 2, 512, seed=2)
+    p = oracle.Problem(cal.cu_seqlens, cal.cu_seqlens_comp, cal.total_tokens, cal.capacity, 4, 2, 512)
+    t0 = time.perf_counter()
+    oracle.fwd32(p, cal.kv, cal.score, cal.ape)
+    oracle.bwd32(p, cal.kv, cal.score, cal.ape, cal.grad_out)
+    per_token = (time.perf_counter() - t0) / cal.total_tokens
+    per_step_s = max(0.02, 120.0 / max(1, steps + warm))
+    tokens = int(max(64, min(case.total_tokens, per_step_s / per_token)))
+    lens, acc = [], 0
+    for L in case.seqlens:
+        take = int(min(L, tokens - acc))
+        if take <= 0:
+            break
+        lens.append(take)
+        acc += take
+    sample = workloads.make_case("ref", lens, 4, 2, 512, pad_rows=max(0, round(1024 * acc / case.total_tokens)),
+                                 seed=3)
+    sp = oracle.Problem(sample.cu_seqlens, sample.cu_seqlens_comp, sample.total_tokens, sample.capacity,
+                        4, 2, 512)
+
+    def step():
+        oracle.fwd32(sp, sample.kv, sample.score, sample.ape)
+        oracle.bwd32(sp, sample.kv, sample.score, sample.ape, sample.grad_out)
+
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t0
+    value = sample.total_tokens * steps / el
+    desc = (f"per step: first {len(lens)} segments of the headline workload ({sample.total_tokens} tokens), "
+            f"O32 fwd + bwd on all {cores} host cores")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import gated_softmax_kv_gb300 as gsk
+    import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    gsk.build()
+    lib = gsk.load()  # noqa: F841  (fails loudly if the library is missing)
+    case = headline_case(args.tokens, seed=rank)
+    T, C, r, coff, d = case.total_tokens, case.capacity, case.ratio, case.coff, case.head_dim
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    kv, score, grad_out = up(case.kv), up(case.score), up(case.grad_out)
+    ape = torch.from_numpy(case.ape).to(dev)
+    cu = torch.from_numpy(case.cu_seqlens).to(dev)
+    cuc = torch.from_numpy(case.cu_seqlens_comp).to(dev)
+    out = torch.empty((C, d), dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty_like(kv)
+    dscore = torch.empty_like(score)
+    dape = torch.empty_like(ape)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    nseq = case.num_seqs
+
+    def fwd():
+        gsk.csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
+                                 cuc.data_ptr(), nseq, T, C, r, coff, d, out.data_ptr(), sh)
+
+    def bwd():
+        gsk.csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
+                                 cuc.data_ptr(), nseq, T, C, r, coff, d, grad_out.data_ptr(),
+                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    if pg is not None:
+        t = torch.tensor([elapsed], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    # end to end through the same C ABI with host buffers: pinned host -> HBM
+    # copies of every input, both calls, and every result back to the host
+    h_kv = torch.empty(kv.shape, dtype=torch.bfloat16, pin_memory=True).copy_(kv)
+    h_score = torch.empty(score.shape, dtype=torch.bfloat16, pin_memory=True).copy_(score)
+    h_go = torch.empty(grad_out.shape, dtype=torch.bfloat16, pin_memory=True).copy_(grad_out)
+    h_ape = torch.empty(ape.shape, dtype=torch.float32, pin_memory=True).copy_(ape)
+    h_cu = torch.empty(cu.shape, dtype=torch.int32, pin_memory=True).copy_(cu)
+    h_cuc = torch.empty(cuc.shape, dtype=torch.int32, pin_memory=True).copy_(cuc)
+    h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    h_dkv = torch.empty(dkv.shape, dtype=torch.bfloat16, pin_memory=True)
+    h_ds = torch.empty(dscore.shape, dtype=torch.bfloat16, pin_memory=True)
+    h_dape = torch.empty(dape.shape, dtype=torch.float32, pin_memory=True)
+    ins = [(kv, h_kv), (score, h_score), (grad_out, h_go), (ape, h_ape), (cu, h_cu), (cuc, h_cuc)]
+    outs = [(out, h_out), (dkv, h_dkv), (dscore, h_ds), (dape, h_dape)]
+    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
+
+    def e2e_step():
+        for dt, ht in ins:
+            dt.copy_(ht, non_blocking=True)
+        fwd()
+        bwd()
+        for dt, ht in outs:
+            ht.copy_(dt, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    KE = max(1, args.e2e_steps)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if pg is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    barrier()
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    fwd_bytes, bwd_bytes = algorithmic_bytes(case)
+    peak, peak_src = measured_peak()
+    fwd_avg = statistics.mean(fwd_ms) / 1e3
+    bwd_avg = statistics.mean(bwd_ms) / 1e3
+    fwd_gbs = fwd_bytes / fwd_avg / 1e9
+    bwd_gbs = bwd_bytes / bwd_avg / 1e9
+    value = T * K * world / elapsed
+    dominant = "bwd" if bwd_avg >= fwd_avg else "fwd"
+    dom_bytes, dom_gbs = (bwd_bytes, bwd_gbs) if dominant == "bwd" else (fwd_bytes, fwd_gbs)
+    traffic = ncu_traffic("csa_compress_bwd" if dominant == "bwd" else "csa_compress_fwd", T)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc, _ = oracle_rate(case)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, the page's gate distribution)",
+        "config": {"workload": WORKLOAD if T == 262144 else f"headline recipe scaled to {T} tokens", "tokens": T, "true_rows": case.true_rows, "capacity": C,
+                   "ratio": r, "coff": coff, "head_dim": d, "segments": case.num_seqs,
+                   "l2": "inputs larger than L2 (kv+score 1 GiB per step), no flush",
+                   "step": "csa_compress_fwd + csa_compress_bwd (3 kernels)"},
+        "roofline": {"bound": "hbm", "kernel": "csa_compress_" + dominant + (" (bwd kernel + dape reduce)" if dominant == "bwd" else ""),
+                     "achieved": dom_gbs, "peak": peak, "unit": "GB/s", "frac": dom_gbs / peak,
+                     "traffic": traffic, "algorithmic_bytes": dom_bytes, "peak_source": peak_src},
+        "fwd": {"ms": fwd_avg * 1e3, "tokens_per_s": T / fwd_avg, "GBps": fwd_gbs, "frac": fwd_gbs / peak,
+                "algorithmic_bytes": fwd_bytes},
+        "bwd": {"ms": bwd_avg * 1e3, "tokens_per_s": T / bwd_avg, "GBps": bwd_gbs, "frac": bwd_gbs / peak,
+                "algorithmic_bytes": bwd_bytes},
+        "e2e": {"value": T * KE * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": KE},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+"""Python binding of the C ABI in include/csa_compress.h (argument marshalling only).
+
+Every computation runs in libcsa_compress.so; this module checks tensor
+dtypes/devices/shapes, derives the sizes the C calls want from tensor shapes,
+and raises ``CsaError`` on a nonzero status. There is no CPU or eager
+fallback: if the library is missing the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+CSA_STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_ALIGN", 3: "CSA_ERR_UNSUPPORTED",
+              4: "CSA_ERR_RANGE", 5: "CSA_ERR_CUDA"}
+
+_lib = None
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        name = CSA_STATUS.get(status, str(status))
+        super().__init__(f"{name}: {detail}")
+
+
+def load() -> ctypes.CDLL:
+    """Load libcsa_compress.so (built by ``gated_softmax_kv_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    common = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32]
+    lib.csa_compress_fwd.argtypes = common + [vp, vp]
+    lib.csa_compress_fwd.restype = ctypes.c_int
+    lib.csa_compress_bwd.argtypes = common + [vp, vp, vp, vp, vp]
+    lib.csa_compress_bwd.restype = ctypes.c_int
+    lib.csa_status_string.argtypes = [ctypes.c_int]
+    lib.csa_status_string.restype = ctypes.c_char_p
+    lib.csa_last_cuda_error.argtypes = []
+    lib.csa_last_cuda_error.restype = i32
+    _lib = lib
+    return lib
+
+
+def _raise(status: int):
+    lib = load()
+    detail = lib.csa_status_string(status).decode()
+    if status == 5:
+        detail += f" (cudaError {lib.csa_last_cuda_error()})"
+    raise CsaError(status, detail)
+
+
+# ------------------------------------------------------------- raw pointers
+
+
+def csa_compress_fwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seqlens_comp: int,
+                         num_seqs: int, total_tokens: int, capacity: int, ratio: int, coff: int,
+                         head_dim: int, out: int, stream: int = 0) -> None:
+    st = load().csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs,
+                                 total_tokens, capacity, ratio, coff, head_dim, out, stream)
+    if st != 0:
+        _raise(st)
+
+
+def csa_compress_bwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seqlens_comp: int,
+                         num_seqs: int, total_tokens: int, capacity: int, ratio: int, coff: int,
+                         head_dim: int, grad_out: int, dkv: int, dscore: int, dape: int,
+                         stream: int = 0) -> None:
+    st = load().csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs,
+                                 total_tokens, capacity, ratio, coff, head_dim, grad_out, dkv,
+                                 dscore, dape, stream)
+    if st != 0:
+        _raise(st)
+
+
+# ------------------------------------------------------------- torch tensors
+
+
+def _check(t, name, dtype, device, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim):
+    import torch
+    dev = kv.device
+    _check(kv, "kv", torch.bfloat16, dev, 2)
+    _check(score, "score", torch.bfloat16, dev, 2)
+    _check(ape, "ape", torch.float32, dev, 2)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    _check(cu_seqlens_comp, "cu_seqlens_comp", torch.int32, dev, 1)
+    if kv.shape != score.shape or kv.shape[1] != coff * head_dim:
+        raise ValueError("kv and score must both be [total_tokens, coff*head_dim]")
+    if tuple(ape.shape) != (ratio, coff * head_dim):
+        raise ValueError("ape must be [ratio, coff*head_dim]")
+    if cu_seqlens.shape != cu_seqlens_comp.shape or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens and cu_seqlens_comp must both be [num_seqs + 1]")
+    return dev, int(cu_seqlens.numel() - 1), int(kv.shape[0])
+
+
+def csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int, ratio: int,
+                     coff: int, head_dim: int, out=None, stream=None):
+    """Forward on device tensors; returns out [capacity, head_dim] bf16."""
+    import torch
+    dev, nseq, T = _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim)
+    if out is None:
+        out = torch.empty((capacity, head_dim), dtype=torch.bfloat16, device=dev)
+    _check(out, "out", torch.bfloat16, dev, 2)
+    if tuple(out.shape) != (capacity, head_dim):
+        raise ValueError("out must be [capacity, head_dim]")
+    csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu_seqlens.data_ptr(),
+                         cu_seqlens_comp.data_ptr(), nseq, T, capacity, ratio, coff, head_dim,
+                         out.data_ptr(), _stream_handle(stream, dev))
+    return out
+
+
+def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int, ratio: int,
+                     coff: int, head_dim: int, grad_out, dkv=None, dscore=None, dape=None,
+                     stream=None):
+    """Backward on device tensors; returns (dkv, dscore, dape). dkv/dscore may be
+    uninitialised; dape is overwritten."""
+    import torch
+    dev, nseq, T = _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim)
+    _check(grad_out, "grad_out", torch.bfloat16, dev, 2)
+    if tuple(grad_out.shape) != (capacity, head_dim):
+        raise ValueError("grad_out must be [capacity, head_dim]")
+    if dkv is None:
+        dkv = torch.empty_like(kv)
+    if dscore is None:
+        dscore = torch.empty_like(score)
+    if dape is None:
+        dape = torch.empty_like(ape)
+    _check(dkv, "dkv", torch.bfloat16, dev, 2)
+    _check(dscore, "dscore", torch.bfloat16, dev, 2)
+    _check(dape, "dape", torch.float32, dev, 2)
+    if dkv.shape != kv.shape or dscore.shape != kv.shape or dape.shape != ape.shape:
+        raise ValueError("gradient buffers must match kv / score / ape")
+    csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu_seqlens.data_ptr(),
+                         cu_seqlens_comp.data_ptr(), nseq, T, capacity, ratio, coff, head_dim,
+                         grad_out.data_ptr(), dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(),
+                         _stream_handle(stream, dev))
+    return dkv, dscore, dape

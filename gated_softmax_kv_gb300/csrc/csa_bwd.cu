@@ -1,0 +1,576 @@
+// Backward kernels of the CSA/HCA fused Compressor for sm_103a.
+//
+// cuDNN-frontend "CSA Fused Compressor", sections "Semantics" and "Class API":
+// with p the softmax weights of a row's window, g = grad_out[b, j],
+//   dp_k = g * kv_k,  S = sum_k dp_k * p_k,
+//   dscore_k = p_k * (dp_k - S),  dkv_k = g * p_k,  dape[k % ratio, c] += dscore_k.
+// dkv / dscore are written in full: every position a non-padding row reads
+// gets its gradient from that row (the unique reader), every other position
+// gets +0 from a unique owner -- the segment's last row owns its block's
+// unread first-half columns and the segment tail, and a sweep over segments
+// shorter than `ratio` and over tokens >= cu_seqlens[-1] owns the rest.
+// Padding rows (b >= cu_seqlens_comp[-1]) are not visited at all.
+//
+// dape is reduced deterministically in two levels, without atomics: each CTA
+// accumulates its rows' logit gradients in registers (rows in a fixed order),
+// combines its threads in a fixed order and writes one fp32 partial per row
+// group; dape_reduce then sums the partials in group order and overwrites dape.
+//
+// Kernel shapes mirror the forward (csa_fwd.cu): bwd_small keeps a W <= 8
+// window per thread in registers and reproduces the plain eager operation
+// order exactly; bwd_chunk splits W >= 16 windows over threadIdx.y chunks of
+// 8 slots and merges the per-chunk (max, sum exp) and S partials in a fixed
+// order through shared memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kKpt = 8;   // window slots per thread in the chunked kernel
+constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
+
+__device__ __forceinline__ uint2 ld_stream8(const uint16_t* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ void st_stream8(uint16_t* p, uint2 v) {
+  __stcs(reinterpret_cast<uint2*>(p), v);
+}
+
+// Zeros for the positions no row reads that belong to nobody's window:
+// segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
+// Spread over every CTA of the launch.
+__device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
+  const Problem& p = bp.p;
+  const int64_t ld = (int64_t)p.coff * p.d;
+  const int64_t vpt = ld / kVec;  // 16-byte vectors per token row
+  const int nthr = blockDim.x * blockDim.y;
+  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+  const int64_t fb = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+  const int64_t nb = (int64_t)gridDim.x * gridDim.y;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t s = fb; s < p.nseq; s += nb) {
+    int64_t lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
+    if (hi - lo >= ratio || hi <= lo) continue;
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > p.T ? p.T : hi;
+    for (int64_t v = lo * vpt + tid; v < hi * vpt; v += nthr) {
+      st_stream(bp.dkv + v * kVec, zero);
+      st_stream(bp.dscore + v * kVec, zero);
+    }
+  }
+  int64_t end = __ldg(p.cu + p.nseq);
+  end = end < 0 ? 0 : (end > p.T ? p.T : end);
+  for (int64_t v = end * vpt + fb * nthr + tid; v < p.T * vpt; v += nb * nthr) {
+    st_stream(bp.dkv + v * kVec, zero);
+    st_stream(bp.dscore + v * kVec, zero);
+  }
+}
+
+template <int R, int COFF>
+__global__ void __launch_bounds__(kThreads)
+bwd_small_kernel(const BwdParams bp) {
+  constexpr int W = COFF * R;
+  using S = Slot<R, COFF>;
+  const Problem& p = bp.p;
+  const int TX = blockDim.x, TY = blockDim.y;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx, nthr = TX * TY;
+  const int nvec = p.d / kVec;
+  const int jv = blockIdx.x * TX + tx;
+  const bool col_ok = jv < nvec;
+  const int64_t ld = (int64_t)COFF * p.d;
+  const int j0 = jv * kVec;
+  const int tile_cols = TX * kVec;
+
+  // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
+  extern __shared__ float sm[];
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    sm[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
+  }
+  __syncthreads();
+  const float* ape_s = sm + tx * kVec;
+
+  float dacc[W][kVec];
+#pragma unroll
+  for (int k = 0; k < W; ++k)
+#pragma unroll
+    for (int c = 0; c < kVec; ++c) dacc[k][c] = 0.0f;
+
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t stride = (int64_t)gridDim.y * TY;
+  for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
+    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
+    const bool has_grad = b < p.C;                    // rows past capacity have no output slot
+    uint4 kvv[W], scv[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(ri.first, k)) {
+        kvv[k] = zero;
+        scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      } else {
+        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
+        kvv[k] = ld_stream(p.kv + off);
+        scv[k] = ld_stream(p.score + off);
+      }
+    }
+    const uint4 gv = has_grad ? ld_stream(bp.grad_out + b * p.d + j0) : zero;
+
+    uint32_t dkw[W][4], dzw[W][4];
+#pragma unroll
+    for (int c2 = 0; c2 < 4; ++c2) {
+      float dk2[W][2], dz2[W][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * c2 + h;
+        float z[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), ape_s[k * tile_cols + c]);
+        float m = z[0];
+#pragma unroll
+        for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
+        float pk[W];
+        float den = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          pk[k] = expf(__fsub_rn(z[k], m));
+          den = __fadd_rn(den, pk[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) pk[k] = __fdiv_rn(pk[k], den);
+        const float g = bf16_elem(gv, c);
+        float dp[W];
+        float sum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          dp[k] = __fmul_rn(g, bf16_elem(kvv[k], c));
+          sum = __fadd_rn(sum, __fmul_rn(dp[k], pk[k]));
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const float dz = __fmul_rn(pk[k], __fsub_rn(dp[k], sum));
+          const float dk = __fmul_rn(g, pk[k]);
+          dz2[k][h] = has_grad ? dz : 0.0f;
+          dk2[k][h] = has_grad ? dk : 0.0f;
+          if (has_grad) dacc[k][c] = __fadd_rn(dacc[k][c], dz);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        dkw[k][c2] = pack_bf16x2(dk2[k][0], dk2[k][1]);
+        dzw[k][c2] = pack_bf16x2(dz2[k][0], dz2[k][1]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(ri.first, k)) continue;
+      const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
+      st_stream(bp.dkv + off, make_uint4(dkw[k][0], dkw[k][1], dkw[k][2], dkw[k][3]));
+      st_stream(bp.dscore + off, make_uint4(dzw[k][0], dzw[k][1], dzw[k][2], dzw[k][3]));
+    }
+    if (ri.last) {
+      // the segment's last row owns its block's unread first-half columns ...
+      if (COFF == 2) {
+#pragma unroll
+        for (int t = 0; t < R; ++t) {
+          const int64_t off = (ri.base + t) * ld + j0;
+          st_stream(bp.dkv + off, zero);
+          st_stream(bp.dscore + off, zero);
+        }
+      }
+      // ... and the segment's tail tokens (seqlen % ratio of them)
+      const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
+      for (int64_t tok = ri.base + R; tok < tail_end; ++tok) {
+#pragma unroll
+        for (int h = 0; h < COFF; ++h) {
+          const int64_t off = tok * ld + h * p.d + j0;
+          st_stream(bp.dkv + off, zero);
+          st_stream(bp.dscore + off, zero);
+        }
+      }
+    }
+  }
+
+  zero_orphans(bp, R);
+
+  // combine the TY thread rows in ascending order, then write this CTA's
+  // slice of the partial of row group blockIdx.y
+  __syncthreads();
+  for (int t = 0; t < TY; ++t) {
+    if (ty == t && col_ok) {
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+#pragma unroll
+        for (int c = 0; c < kVec; ++c) {
+          float* s = sm + k * tile_cols + tx * kVec + c;
+          *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
+        }
+    }
+    __syncthreads();
+  }
+  float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    if (col < p.d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col] = sm[i];
+  }
+}
+
+// Chunked window: blockDim = (TX, TY), TY = W / kKpt; a thread owns 8 slots
+// x 4 columns; the CTA walks rows b = blockIdx.y, blockIdx.y + gridDim.y, ...
+template <int R, int COFF>
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_chunk_kernel(const BwdParams bp) {
+  constexpr int W = COFF * R;
+  constexpr int TY = W / kKpt;
+  using S = Slot<R, COFF>;
+  const Problem& p = bp.p;
+  const int TX = blockDim.x;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx, nthr = TX * TY;
+  const int ncv = p.d / kCv;
+  const int cv = blockIdx.x * TX + tx;
+  const bool col_ok = cv < ncv;
+  const int64_t ld = (int64_t)COFF * p.d;
+  const int j0 = cv * kCv;
+  const int k0 = ty * kKpt;
+  const int tile_cols = TX * kCv;
+  const float kNegInf = __int_as_float(0xff800000);
+
+  extern __shared__ float sm[];
+  float* ape_s = sm;                            // [W][tile_cols]
+  float* m_s = ape_s + W * tile_cols;           // [TY][tile_cols] chunk max
+  float* d_s = m_s + TY * tile_cols;            // [TY][tile_cols] chunk sum exp
+  float* s_s = d_s + TY * tile_cols;            // [TY][tile_cols] chunk S
+  float* M_s = s_s + TY * tile_cols;            // [tile_cols] merged max
+  float* D_s = M_s + tile_cols;                 // [tile_cols] merged den
+  float* S_s = D_s + tile_cols;                 // [tile_cols] merged S
+
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    ape_s[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
+  }
+  __syncthreads();
+
+  float dacc[kKpt][kCv];
+#pragma unroll
+  for (int kk = 0; kk < kKpt; ++kk)
+#pragma unroll
+    for (int c = 0; c < kCv; ++c) dacc[kk][c] = 0.0f;
+
+  const uint2 zero2 = make_uint2(0u, 0u);
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  for (int64_t b = blockIdx.y; b < true_rows; b += gridDim.y) {
+    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // uniform over the CTA
+    const bool has_grad = b < p.C;
+    const bool chunk_masked = S::masked(ri.first, k0);
+    const bool active = col_ok && !chunk_masked;
+    const int64_t base_off = S::tok(ri.base, k0) * ld + S::half(k0) * p.d + j0;
+
+    // phase 1: chunk max and sum of exp
+    uint2 kvv[kKpt], scv[kKpt];
+    float mloc[kCv], dloc[kCv];
+    if (active) {
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        kvv[kk] = ld_stream8(p.kv + base_off + kk * ld);
+        scv[kk] = ld_stream8(p.score + base_off + kk * ld);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        kvv[kk] = zero2;
+        scv[kk] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+      }
+    }
+    float z[kKpt][kCv];
+#pragma unroll
+    for (int c = 0; c < kCv; ++c) {
+      const uint32_t sh = c < 2 ? 0 : 1;
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        const uint32_t w = sh ? scv[kk].y : scv[kk].x;
+        z[kk][c] = __fadd_rn(bf16_at(w, c & 1), ape_s[(k0 + kk) * tile_cols + tx * kCv + c]);
+      }
+      float m = z[0][c];
+#pragma unroll
+      for (int kk = 1; kk < kKpt; ++kk) m = max_nan(m, z[kk][c]);
+      float den = 0.0f;
+      if (m != kNegInf) {
+#pragma unroll
+        for (int kk = 0; kk < kKpt; ++kk) den = __fadd_rn(den, expf(__fsub_rn(z[kk][c], m)));
+      }
+      mloc[c] = m;
+      dloc[c] = den;
+    }
+    {
+      float4* mw = reinterpret_cast<float4*>(m_s + ty * tile_cols + tx * kCv);
+      float4* dw = reinterpret_cast<float4*>(d_s + ty * tile_cols + tx * kCv);
+      *mw = make_float4(mloc[0], mloc[1], mloc[2], mloc[3]);
+      *dw = make_float4(dloc[0], dloc[1], dloc[2], dloc[3]);
+    }
+    __syncthreads();
+    for (int cc = tid; cc < tile_cols; cc += nthr) {
+      float M = m_s[cc];
+      for (int y = 1; y < TY; ++y) M = max_nan(M, m_s[y * tile_cols + cc]);
+      float den = 0.0f;
+      for (int y = 0; y < TY; ++y)
+        den = __fadd_rn(den, __fmul_rn(d_s[y * tile_cols + cc],
+                                       expf(__fsub_rn(m_s[y * tile_cols + cc], M))));
+      M_s[cc] = M;
+      D_s[cc] = den;
+    }
+    __syncthreads();
+
+    // phase 2: weights and the chunk's share of S
+    const uint2 gv = (has_grad && col_ok) ? ld_stream8(bp.grad_out + b * p.d + j0) : zero2;
+    float pk[kKpt][kCv];
+    float sloc[kCv];
+#pragma unroll
+    for (int c = 0; c < kCv; ++c) {
+      const float M = M_s[tx * kCv + c];
+      const float D = D_s[tx * kCv + c];
+      const float g = bf16_at(c < 2 ? gv.x : gv.y, c & 1);
+      float s = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        pk[kk][c] = __fdiv_rn(expf(__fsub_rn(z[kk][c], M)), D);
+        const float x = bf16_at(c < 2 ? kvv[kk].x : kvv[kk].y, c & 1);
+        s = __fadd_rn(s, __fmul_rn(__fmul_rn(g, x), pk[kk][c]));
+      }
+      sloc[c] = s;
+    }
+    *reinterpret_cast<float4*>(s_s + ty * tile_cols + tx * kCv) =
+        make_float4(sloc[0], sloc[1], sloc[2], sloc[3]);
+    __syncthreads();
+    for (int cc = tid; cc < tile_cols; cc += nthr) {
+      float s = 0.0f;
+      for (int y = 0; y < TY; ++y) s = __fadd_rn(s, s_s[y * tile_cols + cc]);
+      S_s[cc] = s;
+    }
+    __syncthreads();
+
+    // phase 3: gradients, stores, dape accumulation
+    uint32_t dkw[kKpt][2], dzw[kKpt][2];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      float dk2[kKpt][2], dz2[kKpt][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * c2 + h;
+        const float sum = S_s[tx * kCv + c];
+        const float g = bf16_at(c2 ? gv.y : gv.x, h);
+#pragma unroll
+        for (int kk = 0; kk < kKpt; ++kk) {
+          const float x = bf16_at(c2 ? kvv[kk].y : kvv[kk].x, h);
+          const float dz = __fmul_rn(pk[kk][c], __fsub_rn(__fmul_rn(g, x), sum));
+          const float dk = __fmul_rn(g, pk[kk][c]);
+          dz2[kk][h] = has_grad ? dz : 0.0f;
+          dk2[kk][h] = has_grad ? dk : 0.0f;
+          if (has_grad) dacc[kk][c] = __fadd_rn(dacc[kk][c], dz);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        dkw[kk][c2] = pack_bf16x2(dk2[kk][0], dk2[kk][1]);
+        dzw[kk][c2] = pack_bf16x2(dz2[kk][0], dz2[kk][1]);
+      }
+    }
+    if (active) {
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        st_stream8(bp.dkv + base_off + kk * ld, make_uint2(dkw[kk][0], dkw[kk][1]));
+        st_stream8(bp.dscore + base_off + kk * ld, make_uint2(dzw[kk][0], dzw[kk][1]));
+      }
+    }
+    if (ri.last) {
+      // unread positions owned by the segment's last row, for this column tile
+      const int tile_cv = TX;
+      const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
+      const int64_t n_first = COFF == 2 ? (int64_t)R * tile_cv : 0;
+      const int64_t n_tail = (tail_end - (ri.base + R)) * COFF * tile_cv;
+      for (int64_t i = tid; i < n_first + n_tail; i += nthr) {
+        int64_t tok;
+        int h, x;
+        if (i < n_first) {
+          tok = ri.base + i / tile_cv;
+          h = 0;
+          x = (int)(i % tile_cv);
+        } else {
+          const int64_t t = i - n_first;
+          tok = ri.base + R + t / (COFF * tile_cv);
+          h = (int)((t / tile_cv) % COFF);
+          x = (int)(t % tile_cv);
+        }
+        const int col_v = blockIdx.x * tile_cv + x;
+        if (col_v >= ncv) continue;
+        const int64_t off = tok * ld + h * p.d + col_v * kCv;
+        st_stream8(bp.dkv + off, zero2);
+        st_stream8(bp.dscore + off, zero2);
+      }
+    }
+  }
+
+  zero_orphans(bp, R);
+
+  // each (slot, column) of the tile belongs to exactly one thread: write the
+  // partial of row group blockIdx.y directly
+  if (col_ok) {
+    float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
+#pragma unroll
+    for (int kk = 0; kk < kKpt; ++kk) {
+      const int k = k0 + kk;
+      float* dst = part + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
+      *reinterpret_cast<float4*>(dst) = make_float4(dacc[kk][0], dacc[kk][1], dacc[kk][2], dacc[kk][3]);
+    }
+  }
+}
+
+// dape[e] = sum over groups g (ascending) of partial[g][e], in two fixed
+// levels: 16 lanes take every 16th group in order, then lane 0 adds the 16
+// lane sums in order.
+__global__ void __launch_bounds__(512)
+dape_reduce_kernel(const float* __restrict__ partial, int32_t groups, int64_t n,
+                   float* __restrict__ dape) {
+  __shared__ float red[16][33];
+  const int64_t e = (int64_t)blockIdx.x * 32 + threadIdx.x;
+  float s = 0.0f;
+  if (e < n) {
+#pragma unroll 4
+    for (int g = threadIdx.y; g < groups; g += 16) s = __fadd_rn(s, __ldcs(partial + (int64_t)g * n + e));
+  }
+  red[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && e < n) {
+    float t = red[0][threadIdx.x];
+    for (int y = 1; y < 16; ++y) t = __fadd_rn(t, red[y][threadIdx.x]);
+    dape[e] = t;
+  }
+}
+
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess ||
+      blocks < 1)
+    blocks = 1;
+  return blocks;
+}
+
+template <int R, int COFF>
+cudaError_t plan_small(const Problem& p, BwdShape* s) {
+  constexpr int W = COFF * R;
+  const int nvec = p.d / kVec;
+  const int tx = nvec <= 128 ? nvec : 128;
+  const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
+  const int tiles = (nvec + tx - 1) / tx;
+  const size_t smem = sizeof(float) * W * tx * kVec;
+  auto kern = bwd_small_kernel<R, COFF>;
+  static bool attr = [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    return true;
+  }();
+  (void)attr;
+  const int occ = occupancy(kern, tx * ty, smem);
+  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  const int64_t row_blocks = (p.C + ty - 1) / ty;
+  if (gy > row_blocks) gy = row_blocks;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  s->grid = dim3(tiles, (unsigned)gy);
+  s->block = dim3(tx, ty);
+  s->smem = smem;
+  s->groups = (int32_t)gy;
+  return cudaSuccess;
+}
+
+template <int R, int COFF>
+cudaError_t plan_chunk(const Problem& p, BwdShape* s) {
+  constexpr int W = COFF * R;
+  constexpr int TY = W / kKpt;
+  const int ncv = p.d / kCv;
+  int tx = kThreads / TY;
+  if (tx > ncv) tx = ncv;
+  const int tiles = (ncv + tx - 1) / tx;
+  const int tile_cols = tx * kCv;
+  const size_t smem = sizeof(float) * ((size_t)W * tile_cols + 3 * (size_t)TY * tile_cols + 3 * tile_cols);
+  auto kern = bwd_chunk_kernel<R, COFF>;
+  static bool attr = [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    return true;
+  }();
+  (void)attr;
+  const int occ = occupancy(kern, tx * TY, smem);
+  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  if (gy > p.C) gy = p.C;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  s->grid = dim3(tiles, (unsigned)gy);
+  s->block = dim3(tx, TY);
+  s->smem = smem;
+  s->groups = (int32_t)gy;
+  return cudaSuccess;
+}
+
+template <int R, int COFF>
+cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
+  bwd_small_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
+  return cudaGetLastError();
+}
+
+template <int R, int COFF>
+cudaError_t run_chunk(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
+  bwd_chunk_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
+  return cudaGetLastError();
+}
+
+#define CSA_BWD_DISPATCH(FN_SMALL, FN_CHUNK, ...)                 \
+  switch (p.ratio * 4 + p.coff) {                                 \
+    case 2 * 4 + 1: return FN_SMALL<2, 1>(__VA_ARGS__);           \
+    case 2 * 4 + 2: return FN_SMALL<2, 2>(__VA_ARGS__);           \
+    case 4 * 4 + 1: return FN_SMALL<4, 1>(__VA_ARGS__);           \
+    case 4 * 4 + 2: return FN_SMALL<4, 2>(__VA_ARGS__);           \
+    case 8 * 4 + 1: return FN_SMALL<8, 1>(__VA_ARGS__);           \
+    case 8 * 4 + 2: return FN_CHUNK<8, 2>(__VA_ARGS__);           \
+    case 16 * 4 + 1: return FN_CHUNK<16, 1>(__VA_ARGS__);         \
+    case 16 * 4 + 2: return FN_CHUNK<16, 2>(__VA_ARGS__);         \
+    case 32 * 4 + 1: return FN_CHUNK<32, 1>(__VA_ARGS__);         \
+    case 32 * 4 + 2: return FN_CHUNK<32, 2>(__VA_ARGS__);         \
+    case 64 * 4 + 1: return FN_CHUNK<64, 1>(__VA_ARGS__);         \
+    case 64 * 4 + 2: return FN_CHUNK<64, 2>(__VA_ARGS__);         \
+    case 128 * 4 + 1: return FN_CHUNK<128, 1>(__VA_ARGS__);       \
+    case 128 * 4 + 2: return FN_CHUNK<128, 2>(__VA_ARGS__);       \
+    default: return cudaErrorInvalidValue;                        \
+  }
+
+}  // namespace
+
+cudaError_t plan_bwd(const Problem& p, BwdShape* shape) {
+  CSA_BWD_DISPATCH(plan_small, plan_chunk, p, shape)
+}
+
+cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
+  const Problem& p = b.p;
+  CSA_BWD_DISPATCH(run_small, run_chunk, b, shape, stream)
+}
+
+cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
+                               cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = (n + 31) / 32;
+  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, 16), 0, stream>>>(partial, groups, n, dape);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,119 @@
+// Device-side building blocks shared by the forward and backward kernels of
+// the CSA/HCA fused Compressor (cuDNN-frontend "CSA Fused Compressor").
+//
+// Numerics (page section "Numerics"): every product, sum and quotient is a
+// separately rounded fp32 operation (__fmul_rn / __fadd_rn / __fsub_rn /
+// __fdiv_rn, so no FMA contraction can change a result), max propagates NaN,
+// bf16 values widen exactly and narrow once with round-to-nearest-even.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa_internal.h"
+
+namespace csa {
+
+constexpr int kVec = 8;                  // bf16 elements per 16-byte vector
+constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
+
+// ---- bf16 <-> fp32 ---------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_at(uint32_t w, int h) { return h ? bf16_hi(w) : bf16_lo(w); }
+
+// Element c (0..7) of a 16-byte vector of bf16.
+__device__ __forceinline__ float bf16_elem(const uint4& v, int c) {
+  const uint32_t w = (c >> 1) == 0 ? v.x : (c >> 1) == 1 ? v.y : (c >> 1) == 2 ? v.z : v.w;
+  return bf16_at(w, c & 1);
+}
+
+// Two fp32 values -> one bf16x2 word (lo at the lower address), nearest-even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// ---- memory ----------------------------------------------------------------
+
+// kv / score / grad_out are read exactly once: streaming (evict-first) loads.
+__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(uint16_t* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+// ---- row -> segment map (page section "Semantics") -------------------------
+
+struct RowInfo {
+  int64_t base;      // first token of the row's own block
+  int64_t seg_end;   // cu_seqlens[s + 1] (0 for padding rows)
+  bool first;        // first block of its segment (or a padding row)
+  bool last;         // last block of its segment
+};
+
+// Row b < true_rows: s = last segment with cu_seqlens_comp[s] <= b (binary
+// search; terminates and stays in [0, num_seqs) whatever the array holds),
+// i = b - cu_seqlens_comp[s], base = cu_seqlens[s] + i * ratio.
+// Row b >= true_rows (static-capacity padding): first block from token 0.
+__device__ __forceinline__ RowInfo row_info(const int32_t* __restrict__ cu,
+                                            const int32_t* __restrict__ cuc, int nseq,
+                                            int64_t b, int64_t true_rows, int ratio) {
+  RowInfo ri;
+  if (b >= true_rows) {
+    ri.base = 0;
+    ri.seg_end = 0;
+    ri.first = true;
+    ri.last = false;
+    return ri;
+  }
+  int lo = 0, hi = nseq;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)__ldg(cuc + mid) <= b) lo = mid; else hi = mid;
+  }
+  const int64_t c0 = __ldg(cuc + lo);
+  const int64_t c1 = __ldg(cuc + lo + 1);
+  const int64_t i = b - c0;
+  ri.base = (int64_t)__ldg(cu + lo) + i * ratio;
+  ri.seg_end = __ldg(cu + lo + 1);
+  ri.first = (i == 0);
+  ri.last = (i == c1 - c0 - 1);
+  return ri;
+}
+
+// Window slot k of a row: token offset from base, column offset (0 or d),
+// APE row; masked when it is a previous-block slot of a first block.
+template <int R, int COFF>
+struct Slot {
+  static __device__ __forceinline__ int64_t tok(int64_t base, int k) {
+    return COFF == 2 ? (k < R ? base - R + k : base + (k - R)) : base + k;
+  }
+  static __device__ __forceinline__ int half(int k) { return (COFF == 2 && k >= R) ? 1 : 0; }
+  static __device__ __forceinline__ int ape_row(int k) { return (COFF == 2 && k >= R) ? k - R : k; }
+  static __device__ __forceinline__ bool masked(bool first, int k) {
+    return COFF == 2 && k < R && first;
+  }
+};
+
+// Every token a row touches must lie in [0, T): false means violated caller
+// preconditions; such a row is skipped rather than read out of bounds.
+template <int R, int COFF>
+__device__ __forceinline__ bool row_in_bounds(const RowInfo& ri, int64_t T) {
+  const int64_t lo = (COFF == 2 && !ri.first) ? ri.base - R : ri.base;
+  return lo >= 0 && ri.base + R <= T;
+}
+
+}  // namespace csa

@@ -1,0 +1,331 @@
+// Forward kernels of the CSA/HCA fused Compressor for sm_103a.
+//
+// cuDNN-frontend "CSA Fused Compressor", section "Semantics":
+//   out[b, j] = sum_k kv[w(b,k), c(k,j)] * softmax_k(score[w(b,k), c(k,j)] + ape[k % ratio, c(k,j)])
+// fp32 throughout, one final bf16 rounding (section "Numerics").
+//
+// The path is a streaming, HBM-bound pooling: each (token, column) element of
+// kv and score is read exactly once (overlapping windows share tokens, never
+// elements, because the two window halves use disjoint column ranges), so
+// there is nothing for tensor cores or shared-memory reuse to win. Two
+// kernel shapes:
+//
+//  * fwd_small (window W = coff*ratio <= 8): a thread owns one output row and
+//    8 consecutive columns. It issues all 2W 16-byte loads of its window up
+//    front (one coalesced 512-byte request per warp per slot), keeps its APE
+//    columns in registers across the rows it visits (persistent grid, rows
+//    strided by the whole grid) and evaluates the plain eager order: m = max z,
+//    e = exp(z - m), den = sum e, p = e / den, out = sum p * kv.
+//
+//  * fwd_chunk (W >= 16, e.g. ratio = 128): a CTA owns one row of a column
+//    tile per step; its threadIdx.y rows split the window into chunks of 8
+//    slots. Each thread reduces its chunk to a (max, sum exp, sum exp*kv)
+//    triple per column, and the triples are merged in a fixed chunk order in
+//    shared memory (double-buffered: one barrier per row). Deterministic; the
+//    merge reorders the sums, as the page's ratio = 128 kernels do.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "csa_device.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kKpt = 8;  // window slots per thread in the chunked kernels
+
+template <int R, int COFF>
+__global__ void __launch_bounds__(kThreads)
+fwd_small_kernel(const FwdParams f) {
+  constexpr int W = COFF * R;
+  using S = Slot<R, COFF>;
+  const Problem& p = f.p;
+  const int nvec = p.d / kVec;
+  const int jv = blockIdx.x * blockDim.x + threadIdx.x;
+  if (jv >= nvec) return;  // no barrier in this kernel
+  const int64_t ld = (int64_t)COFF * p.d;
+  const int j0 = jv * kVec;
+
+  float apev[W][kVec];
+#pragma unroll
+  for (int k = 0; k < W; ++k) {
+    const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
+    const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
+    apev[k][0] = lo.x; apev[k][1] = lo.y; apev[k][2] = lo.z; apev[k][3] = lo.w;
+    apev[k][4] = hi.x; apev[k][5] = hi.y; apev[k][6] = hi.z; apev[k][7] = hi.w;
+  }
+
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t stride = (int64_t)gridDim.y * blockDim.y;
+  for (int64_t b = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; b < p.C; b += stride) {
+    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    uint16_t* dst = f.out + b * p.d + j0;
+    if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
+      st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
+      continue;
+    }
+    uint4 kvv[W], scv[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(ri.first, k)) {  // kv = 0, score = -inf
+        kvv[k] = make_uint4(0u, 0u, 0u, 0u);
+        scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      } else {
+        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
+        kvv[k] = ld_stream(p.kv + off);
+        scv[k] = ld_stream(p.score + off);
+      }
+    }
+    uint32_t ow[4];
+#pragma unroll
+    for (int c2 = 0; c2 < 4; ++c2) {
+      float res[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * c2 + h;
+        float z[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), apev[k][c]);
+        float m = z[0];
+#pragma unroll
+        for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
+        float e[W];
+        float den = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          e[k] = expf(__fsub_rn(z[k], m));
+          den = __fadd_rn(den, e[k]);
+        }
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          acc = __fadd_rn(acc, __fmul_rn(__fdiv_rn(e[k], den), bf16_elem(kvv[k], c)));
+        res[h] = acc;
+      }
+      ow[c2] = pack_bf16x2(res[0], res[1]);
+    }
+    st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+  }
+}
+
+// Chunked window: blockDim = (TX, TY), TY = W / kKpt chunks of 8 slots.
+template <int R, int COFF>
+__global__ void __launch_bounds__(kThreads)
+fwd_chunk_kernel(const FwdParams f) {
+  constexpr int W = COFF * R;
+  constexpr int TY = W / kKpt;
+  using S = Slot<R, COFF>;
+  const Problem& p = f.p;
+  const int TX = blockDim.x;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx;
+  const int nvec = p.d / kVec;
+  const int jv = blockIdx.x * TX + tx;
+  const bool col_ok = jv < nvec;
+  const int64_t ld = (int64_t)COFF * p.d;
+  const int j0 = jv * kVec;
+  const int k0 = ty * kKpt;
+  const int tile_cols = TX * kVec;
+
+  // [2 buffers][3 quantities][TY][tile_cols]
+  extern __shared__ float sm[];
+  const int qstride = TY * tile_cols;
+
+  float apev[kKpt][kVec];
+#pragma unroll
+  for (int kk = 0; kk < kKpt; ++kk) {
+    const int k = k0 + kk;
+    if (col_ok) {
+      const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
+      const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
+      apev[kk][0] = lo.x; apev[kk][1] = lo.y; apev[kk][2] = lo.z; apev[kk][3] = lo.w;
+      apev[kk][4] = hi.x; apev[kk][5] = hi.y; apev[kk][6] = hi.z; apev[kk][7] = hi.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < kVec; ++c) apev[kk][c] = 0.0f;
+    }
+  }
+
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  int buf = 0;
+  for (int64_t b = blockIdx.y; b < p.C; b += gridDim.y, buf ^= 1) {
+    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    const bool ok = row_in_bounds<R, COFF>(ri, p.T);
+    // chunk slots are all < R or all >= R (R is a multiple of 8): one mask test
+    const bool chunk_masked = S::masked(ri.first, k0);
+    float mloc[kVec], dloc[kVec], aloc[kVec];
+#pragma unroll
+    for (int c = 0; c < kVec; ++c) {
+      mloc[c] = -__int_as_float(0x7f800000);
+      dloc[c] = 0.0f;
+      aloc[c] = 0.0f;
+    }
+    if (col_ok && ok && !chunk_masked) {
+      uint4 kvv[kKpt], scv[kKpt];
+#pragma unroll
+      for (int kk = 0; kk < kKpt; ++kk) {
+        const int k = k0 + kk;
+        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
+        kvv[kk] = ld_stream(p.kv + off);
+        scv[kk] = ld_stream(p.score + off);
+      }
+#pragma unroll
+      for (int c = 0; c < kVec; ++c) {
+        float z[kKpt];
+#pragma unroll
+        for (int kk = 0; kk < kKpt; ++kk) z[kk] = __fadd_rn(bf16_elem(scv[kk], c), apev[kk][c]);
+        float m = z[0];
+#pragma unroll
+        for (int kk = 1; kk < kKpt; ++kk) m = max_nan(m, z[kk]);
+        float den = 0.0f, acc = 0.0f;
+        if (m != -__int_as_float(0x7f800000)) {  // an all -inf chunk contributes nothing
+#pragma unroll
+          for (int kk = 0; kk < kKpt; ++kk) {
+            const float e = expf(__fsub_rn(z[kk], m));
+            den = __fadd_rn(den, e);
+            acc = __fadd_rn(acc, __fmul_rn(e, bf16_elem(kvv[kk], c)));
+          }
+        }
+        mloc[c] = m;
+        dloc[c] = den;
+        aloc[c] = acc;
+      }
+    }
+    float* bm = sm + buf * 3 * qstride;
+    float* bd = bm + qstride;
+    float* ba = bd + qstride;
+#pragma unroll
+    for (int c = 0; c < kVec; ++c) {
+      const int idx = ty * tile_cols + tx * kVec + c;
+      bm[idx] = mloc[c];
+      bd[idx] = dloc[c];
+      ba[idx] = aloc[c];
+    }
+    __syncthreads();
+    // merge the TY chunk triples of each column in ascending chunk order; a
+    // thread finishes two adjacent columns and stores one bf16x2 word
+    for (int pr = tid; pr < tile_cols / 2; pr += TX * TY) {
+      const int cc = 2 * pr;
+      const int col = blockIdx.x * tile_cols + cc;
+      if (col >= p.d) continue;
+      float res[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float M = bm[cc + h];
+        for (int y = 1; y < TY; ++y) M = max_nan(M, bm[y * tile_cols + cc + h]);
+        float den = 0.0f, acc = 0.0f;
+        for (int y = 0; y < TY; ++y) {
+          const float s = expf(__fsub_rn(bm[y * tile_cols + cc + h], M));
+          den = __fadd_rn(den, __fmul_rn(bd[y * tile_cols + cc + h], s));
+          acc = __fadd_rn(acc, __fmul_rn(ba[y * tile_cols + cc + h], s));
+        }
+        res[h] = __fdiv_rn(acc, den);
+      }
+      uint32_t w = pack_bf16x2(res[0], res[1]);
+      if (!ok) w = 0x7FC07FC0u;
+      *reinterpret_cast<uint32_t*>(f.out + b * p.d + col) = w;
+    }
+  }
+}
+
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess ||
+      blocks < 1)
+    blocks = 1;
+  return blocks;
+}
+
+template <int R, int COFF>
+cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
+  const int nvec = f.p.d / kVec;
+  const int tx = nvec <= 128 ? nvec : 128;
+  const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
+  const int tiles = (nvec + tx - 1) / tx;
+  auto kern = fwd_small_kernel<R, COFF>;
+  static int occ = occupancy(kern, tx * ty, 0);
+  const int64_t row_blocks = (f.p.C + ty - 1) / ty;
+  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  if (gy < 1) gy = 1;
+  if (gy > row_blocks) gy = row_blocks;
+  if (gy > 65535) gy = 65535;
+  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, ty), 0, stream>>>(f);
+  return cudaGetLastError();
+}
+
+template <int R, int COFF>
+cudaError_t launch_chunk(const FwdParams& f, cudaStream_t stream) {
+  constexpr int W = COFF * R;
+  constexpr int TY = W / kKpt;
+  const int nvec = f.p.d / kVec;
+  int tx = kThreads / TY;
+  if (tx > nvec) tx = nvec;
+  const int tiles = (nvec + tx - 1) / tx;
+  const size_t smem = sizeof(float) * 2 * 3 * TY * tx * kVec;
+  auto kern = fwd_chunk_kernel<R, COFF>;
+  static bool attr = [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    return true;
+  }();
+  (void)attr;
+  const int occ = occupancy(kern, tx * TY, smem);
+  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  if (gy < 1) gy = 1;
+  if (gy > f.p.C) gy = f.p.C;
+  if (gy > 65535) gy = 65535;
+  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, TY), smem, stream>>>(f);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool supported(int ratio, int coff) {
+  if (coff != 1 && coff != 2) return false;
+  switch (ratio) {
+    case 2: case 4: case 8: case 16: case 32: case 64: case 128: return true;
+    default: return false;
+  }
+}
+
+cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
+  if (f.p.C == 0) return cudaSuccess;
+  const int key = f.p.ratio * 4 + f.p.coff;
+  switch (key) {
+    case 2 * 4 + 1: return launch_small<2, 1>(f, stream);
+    case 2 * 4 + 2: return launch_small<2, 2>(f, stream);
+    case 4 * 4 + 1: return launch_small<4, 1>(f, stream);
+    case 4 * 4 + 2: return launch_small<4, 2>(f, stream);
+    case 8 * 4 + 1: return launch_small<8, 1>(f, stream);
+    case 8 * 4 + 2: return launch_chunk<8, 2>(f, stream);
+    case 16 * 4 + 1: return launch_chunk<16, 1>(f, stream);
+    case 16 * 4 + 2: return launch_chunk<16, 2>(f, stream);
+    case 32 * 4 + 1: return launch_chunk<32, 1>(f, stream);
+    case 32 * 4 + 2: return launch_chunk<32, 2>(f, stream);
+    case 64 * 4 + 1: return launch_chunk<64, 1>(f, stream);
+    case 64 * 4 + 2: return launch_chunk<64, 2>(f, stream);
+    case 128 * 4 + 1: return launch_chunk<128, 1>(f, stream);
+    case 128 * 4 + 2: return launch_chunk<128, 2>(f, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace csa

@@ -1,0 +1,60 @@
+// Internal interface between the C ABI (csa_api.cu) and the kernel
+// translation units (csa_fwd.cu, csa_bwd.cu). Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+// One Compressor call after host validation. Pointers are device pointers;
+// bf16 tensors travel as raw 16-bit patterns.
+struct Problem {
+  const uint16_t* kv;      // [T, coff*d]
+  const uint16_t* score;   // [T, coff*d]
+  const float* ape;        // [ratio, coff*d]
+  const int32_t* cu;       // [nseq + 1]
+  const int32_t* cuc;      // [nseq + 1]
+  int32_t nseq;
+  int32_t ratio;
+  int32_t coff;
+  int32_t d;               // head_dim
+  int64_t T;               // total_tokens
+  int64_t C;               // capacity
+};
+
+struct FwdParams {
+  Problem p;
+  uint16_t* out;           // [C, d]
+};
+
+struct BwdParams {
+  Problem p;
+  const uint16_t* grad_out;  // [C, d]
+  uint16_t* dkv;             // [T, coff*d]
+  uint16_t* dscore;          // [T, coff*d]
+  float* partial;            // [groups, ratio * coff * d] dape partials
+  int32_t groups;            // row groups = number of partials
+};
+
+// Launch shape of the backward: how many dape partials it writes.
+struct BwdShape {
+  dim3 grid;
+  dim3 block;
+  size_t smem;
+  int32_t groups;
+};
+
+bool supported(int ratio, int coff);
+
+cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream);
+
+cudaError_t plan_bwd(const Problem& p, BwdShape* shape);
+cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
+cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
+                               cudaStream_t stream);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+}  // namespace csa

@@ -1,0 +1,86 @@
+"""Device plumbing for the GPU parity tests: upload a seeded case, run the
+C-ABI calls into NaN-prefilled, canary-guarded buffers, download the results."""
+from __future__ import annotations
+
+import numpy as np
+
+import gated_softmax_kv_gb300 as gsk
+
+GUARD = 2048          # bf16 elements (4 KiB) of canary on each side of an output
+CANARY_BF16 = 0x5A5A
+CANARY_F32 = 0x5A5A5A5A
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def dev_bf16(a: np.ndarray):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_bits(t) -> np.ndarray:
+    torch = torch_mod()
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class Guarded:
+    """A device buffer with canary words on both sides; `.inner` is the view
+    handed to the library (16-byte aligned)."""
+
+    def __init__(self, shape, dtype, fill_bits: int):
+        torch = torch_mod()
+        n = int(np.prod(shape))
+        if dtype == "bf16":
+            self.full = torch.full((n + 2 * GUARD,), CANARY_BF16, dtype=torch.int16, device="cuda")
+            self.full[GUARD:GUARD + n] = int(np.uint16(fill_bits).view(np.int16))
+            self.inner = self.full[GUARD:GUARD + n].view(torch.bfloat16).view(*shape)
+        else:
+            self.full = torch.full((n + 2 * GUARD,), CANARY_F32, dtype=torch.int32, device="cuda")
+            self.full[GUARD:GUARD + n] = int(np.uint32(fill_bits).view(np.int32))
+            self.inner = self.full[GUARD:GUARD + n].view(torch.float32).view(*shape)
+        self.n = n
+        self.canary = CANARY_BF16 if dtype == "bf16" else CANARY_F32
+
+    def guards_intact(self) -> bool:
+        head = self.full[:GUARD].cpu().numpy()
+        tail = self.full[GUARD + self.n:].cpu().numpy()
+        c = np.array(self.canary).astype(head.dtype)
+        return bool(np.all(head == c) and np.all(tail == c))
+
+
+class DeviceCase:
+    def __init__(self, case):
+        torch = torch_mod()
+        self.case = case
+        self.kv = dev_bf16(case.kv)
+        self.score = dev_bf16(case.score)
+        self.ape = torch.from_numpy(np.ascontiguousarray(case.ape)).cuda()
+        self.cu = torch.from_numpy(case.cu_seqlens.astype(np.int32)).cuda()
+        self.cuc = torch.from_numpy(case.cu_seqlens_comp.astype(np.int32)).cuda()
+        self.grad_out = dev_bf16(case.grad_out)
+
+    def fwd(self, prefill: int = 0x7FC0):
+        c = self.case
+        out = Guarded((c.capacity, c.head_dim), "bf16", prefill)
+        gsk.csa_compress_fwd(self.kv, self.score, self.ape, self.cu, self.cuc, c.capacity, c.ratio,
+                             c.coff, c.head_dim, out=out.inner)
+        torch_mod().cuda.synchronize()
+        assert out.guards_intact(), "forward wrote outside out"
+        return host_bits(out.inner)
+
+    def bwd(self, prefill: int = 0x7FC0, grad_out=None):
+        torch = torch_mod()
+        c = self.case
+        dkv = Guarded(self.kv.shape, "bf16", prefill)
+        ds = Guarded(self.kv.shape, "bf16", prefill)
+        dape = Guarded(self.ape.shape, "f32", 0x7FC00000 if prefill == 0x7FC0 else prefill << 16)
+        go = self.grad_out if grad_out is None else grad_out
+        gsk.csa_compress_bwd(self.kv, self.score, self.ape, self.cu, self.cuc, c.capacity, c.ratio,
+                             c.coff, c.head_dim, go, dkv=dkv.inner, dscore=ds.inner, dape=dape.inner)
+        torch.cuda.synchronize()
+        assert dkv.guards_intact() and ds.guards_intact() and dape.guards_intact(), \
+            "backward wrote outside its outputs"
+        return host_bits(dkv.inner), host_bits(ds.inner), dape.inner.cpu().numpy()

@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every entry point include/*.h declares, and argument validation
+rejects bad calls before anything touches the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import gated_softmax_kv_gb300 as gsk
+from gated_softmax_kv_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gsk.build()
+    return binding.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(csa_[A-Za-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_two_calls():
+    names = declared_functions()
+    assert "csa_compress_fwd" in names and "csa_compress_bwd" in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        s = lib.csa_status_string(st)
+        assert s and len(s) > 0
+    assert lib.csa_status_string(99) == b"unknown status"
+
+
+# Fake, well-aligned device addresses: validation must reject these calls
+# before any CUDA call is made, so they are never dereferenced.
+A = 0x10000
+
+
+def fwd(lib, **kw):
+    args = dict(kv=A, score=A, ape=A, cu=A, cuc=A, nseq=1, T=64, C=8, r=4, coff=2, d=64, out=A)
+    args.update(kw)
+    return lib.csa_compress_fwd(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
+                                args["nseq"], args["T"], args["C"], args["r"], args["coff"],
+                                args["d"], args["out"], None)
+
+
+def bwd(lib, **kw):
+    args = dict(kv=A, score=A, ape=A, cu=A, cuc=A, nseq=1, T=64, C=8, r=4, coff=2, d=64, go=A,
+                dkv=A, ds=A, dape=A)
+    args.update(kw)
+    return lib.csa_compress_bwd(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
+                                args["nseq"], args["T"], args["C"], args["r"], args["coff"],
+                                args["d"], args["go"], args["dkv"], args["ds"], args["dape"], None)
+
+
+@pytest.mark.parametrize("call", [fwd, bwd])
+def test_validation_rejects_before_launch(lib, call):
+    assert call(lib, r=3) == 3                  # unsupported ratio
+    assert call(lib, r=256) == 3
+    assert call(lib, coff=0) == 3
+    assert call(lib, d=12) == 3                 # head_dim % 8 != 0
+    assert call(lib, d=0) == 3
+    assert call(lib, nseq=0) == 4
+    assert call(lib, T=-1) == 4
+    assert call(lib, C=-1) == 4
+    assert call(lib, T=1 << 21, d=1024) == 4    # T * coff * d >= 2^31
+    assert call(lib, C=1 << 22, d=512) == 4     # capacity * d >= 2^31
+    assert call(lib, T=3, C=1) == 4             # capacity > 0 needs T >= ratio
+    assert call(lib, kv=0) == 1
+    assert call(lib, cu=0) == 1
+    assert call(lib, ape=0) == 1
+    assert call(lib, kv=A + 8) == 2             # 16-byte alignment
+    assert call(lib, ape=A + 4) == 2
+    assert call(lib, cuc=A + 2) == 2            # 4-byte alignment
+
+
+def test_bwd_output_pointers_validated(lib):
+    assert bwd(lib, go=0) == 1
+    assert bwd(lib, dkv=0) == 1
+    assert bwd(lib, dape=0) == 1
+    assert bwd(lib, ds=A + 8) == 2
+    assert fwd(lib, out=0) == 1
+    assert fwd(lib, out=A + 2) == 2
+
+
+def test_fwd_zero_capacity_launches_nothing(lib):
+    # capacity == 0: valid, no launch, no CUDA call (works without a GPU)
+    assert fwd(lib, C=0, out=0) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        binding.load()
