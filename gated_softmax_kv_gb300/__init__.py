@@ -6,7 +6,7 @@ this package holds the kernels (csrc/), their build and a thin Python binding.
 """
 from .binding import (CsaError, csa_compress_bwd, csa_compress_bwd_ptr, csa_compress_fwd,
                       csa_compress_fwd_ptr, load)
-from .build import build
+from .nvbuild import build
 
 __all__ = ["CsaError", "build", "csa_compress_bwd", "csa_compress_bwd_ptr", "csa_compress_fwd",
            "csa_compress_fwd_ptr", "load"]

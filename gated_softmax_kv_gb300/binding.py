@@ -11,7 +11,7 @@ import ctypes
 import os
 from typing import Optional
 
-from . import build as _build
+from . import nvbuild as _build
 
 LIB_PATH = _build.LIB
 
@@ -29,7 +29,7 @@ class CsaError(RuntimeError):
 
 
 def load() -> ctypes.CDLL:
-    """Load libcsa_compress.so (built by ``gated_softmax_kv_gb300.build.build()``)."""
+    """Load libcsa_compress.so (built by ``gated_softmax_kv_gb300.nvbuild.build()``)."""
     global _lib
     if _lib is not None:
         return _lib
