@@ -17,8 +17,8 @@
 // group; dape_reduce then sums the partials in group order and overwrites dape.
 //
 // Kernel shapes mirror the forward (csa_fwd.cu): bwd_small keeps a W <= 8
-// window per thread in registers and reproduces the plain eager operation
-// order exactly; bwd_chunk splits W >= 16 windows over threadIdx.y chunks of
+// window of 4 columns per thread in registers and follows the plain eager
+// operation order (p = e / den per slot, sequential sums); bwd_chunk splits W >= 16 windows over threadIdx.y chunks of
 // 8 slots and merges the per-chunk (max, sum exp) and S partials in a fixed
 // order through shared memory.
 #include <cuda_runtime.h>
@@ -72,8 +72,10 @@ __device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
   }
 }
 
+// Small window (W <= 8): blockDim = (TX, TY); a thread owns 4 consecutive
+// columns (8-byte vectors) of one row at a time, rows strided by the grid.
 template <int R, int COFF>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_small_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
@@ -81,12 +83,12 @@ bwd_small_kernel(const BwdParams bp) {
   const int TX = blockDim.x, TY = blockDim.y;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int tid = ty * TX + tx, nthr = TX * TY;
-  const int nvec = p.d / kVec;
-  const int jv = blockIdx.x * TX + tx;
-  const bool col_ok = jv < nvec;
+  const int ncv = p.d / kCv;
+  const int cv = blockIdx.x * TX + tx;
+  const bool col_ok = cv < ncv;
   const int64_t ld = (int64_t)COFF * p.d;
-  const int j0 = jv * kVec;
-  const int tile_cols = TX * kVec;
+  const int j0 = cv * kCv;
+  const int tile_cols = TX * kCv;
 
   // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
   extern __shared__ float sm[];
@@ -96,86 +98,96 @@ bwd_small_kernel(const BwdParams bp) {
     sm[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
   }
   __syncthreads();
-  const float* ape_s = sm + tx * kVec;
+  const float* ape_s = sm + tx * kCv;
 
-  float dacc[W][kVec];
+  float dacc[W][kCv];
 #pragma unroll
   for (int k = 0; k < W; ++k)
 #pragma unroll
-    for (int c = 0; c < kVec; ++c) dacc[k][c] = 0.0f;
+    for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
 
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint2 zero2 = make_uint2(0u, 0u);
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
   const int64_t stride = (int64_t)gridDim.y * TY;
+  int hint = 0;
   for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
-    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
     const bool has_grad = b < p.C;                    // rows past capacity have no output slot
-    uint4 kvv[W], scv[W];
+    uint2 kvv[W], scv[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) {
       if (S::masked(ri.first, k)) {
-        kvv[k] = zero;
-        scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        kvv[k] = zero2;
+        scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
       } else {
         const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-        kvv[k] = ld_stream(p.kv + off);
-        scv[k] = ld_stream(p.score + off);
+        kvv[k] = ld_stream8(p.kv + off);
+        scv[k] = ld_stream8(p.score + off);
       }
     }
-    const uint4 gv = has_grad ? ld_stream(bp.grad_out + b * p.d + j0) : zero;
+    const uint2 gv = has_grad ? ld_stream8(bp.grad_out + b * p.d + j0) : zero2;
 
-    uint32_t dkw[W][4], dzw[W][4];
+    // z = score + ape, then in place e = exp(z - m), then p = e / den
+    float pz[W][kCv];
 #pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2) {
-      float dk2[W][2], dz2[W][2];
+    for (int k = 0; k < W; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
+      pz[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
+      pz[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
+      pz[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
+      pz[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
+    }
+    uint32_t dkw[W][2], dzw[W][2];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      // both columns of the pair: m, e, den, p, then S
+      float sum[2], g[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = 2 * c2 + h;
-        float z[W];
+        float m = pz[0][c];
 #pragma unroll
-        for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), ape_s[k * tile_cols + c]);
-        float m = z[0];
-#pragma unroll
-        for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
-        float pk[W];
+        for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
         float den = 0.0f;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          pk[k] = expf(__fsub_rn(z[k], m));
-          den = __fadd_rn(den, pk[k]);
+          pz[k][c] = softmax_exp(__fsub_rn(pz[k][c], m));
+          den = __fadd_rn(den, pz[k][c]);
         }
 #pragma unroll
-        for (int k = 0; k < W; ++k) pk[k] = __fdiv_rn(pk[k], den);
-        const float g = bf16_elem(gv, c);
-        float dp[W];
-        float sum = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          dp[k] = __fmul_rn(g, bf16_elem(kvv[k], c));
-          sum = __fadd_rn(sum, __fmul_rn(dp[k], pk[k]));
-        }
+        for (int k = 0; k < W; ++k) pz[k][c] = __fdiv_rn(pz[k][c], den);
+        g[h] = has_grad ? bf16_at(c2 ? gv.y : gv.x, h) : 0.0f;
+        float acc = 0.0f;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          const float dz = __fmul_rn(pk[k], __fsub_rn(dp[k], sum));
-          const float dk = __fmul_rn(g, pk[k]);
-          dz2[k][h] = has_grad ? dz : 0.0f;
-          dk2[k][h] = has_grad ? dk : 0.0f;
-          if (has_grad) dacc[k][c] = __fadd_rn(dacc[k][c], dz);
+          const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+          acc = __fadd_rn(acc, __fmul_rn(dp, pz[k][c]));
         }
+        sum[h] = acc;
       }
+      // dscore = p (dp - S), dkv = g p, packed per slot as soon as both columns exist
 #pragma unroll
       for (int k = 0; k < W; ++k) {
-        dkw[k][c2] = pack_bf16x2(dk2[k][0], dk2[k][1]);
-        dzw[k][c2] = pack_bf16x2(dz2[k][0], dz2[k][1]);
+        float dz[2], dk[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * c2 + h;
+          const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+          dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
+          dk[h] = __fmul_rn(g[h], pz[k][c]);
+          if (has_grad) dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);
+        }
+        dkw[k][c2] = has_grad ? pack_bf16x2(dk[0], dk[1]) : 0u;
+        dzw[k][c2] = has_grad ? pack_bf16x2(dz[0], dz[1]) : 0u;
       }
     }
 #pragma unroll
     for (int k = 0; k < W; ++k) {
       if (S::masked(ri.first, k)) continue;
       const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-      st_stream(bp.dkv + off, make_uint4(dkw[k][0], dkw[k][1], dkw[k][2], dkw[k][3]));
-      st_stream(bp.dscore + off, make_uint4(dzw[k][0], dzw[k][1], dzw[k][2], dzw[k][3]));
+      st_stream8(bp.dkv + off, make_uint2(dkw[k][0], dkw[k][1]));
+      st_stream8(bp.dscore + off, make_uint2(dzw[k][0], dzw[k][1]));
     }
     if (ri.last) {
       // the segment's last row owns its block's unread first-half columns ...
@@ -183,8 +195,8 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
         for (int t = 0; t < R; ++t) {
           const int64_t off = (ri.base + t) * ld + j0;
-          st_stream(bp.dkv + off, zero);
-          st_stream(bp.dscore + off, zero);
+          st_stream8(bp.dkv + off, zero2);
+          st_stream8(bp.dscore + off, zero2);
         }
       }
       // ... and the segment's tail tokens (seqlen % ratio of them)
@@ -193,8 +205,8 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
         for (int h = 0; h < COFF; ++h) {
           const int64_t off = tok * ld + h * p.d + j0;
-          st_stream(bp.dkv + off, zero);
-          st_stream(bp.dscore + off, zero);
+          st_stream8(bp.dkv + off, zero2);
+          st_stream8(bp.dscore + off, zero2);
         }
       }
     }
@@ -210,8 +222,8 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
       for (int k = 0; k < W; ++k)
 #pragma unroll
-        for (int c = 0; c < kVec; ++c) {
-          float* s = sm + k * tile_cols + tx * kVec + c;
+        for (int c = 0; c < kCv; ++c) {
+          float* s = sm + k * tile_cols + tx * kCv + c;
           *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
         }
     }
@@ -309,7 +321,7 @@ bwd_chunk_kernel(const BwdParams bp) {
       float den = 0.0f;
       if (m != kNegInf) {
 #pragma unroll
-        for (int kk = 0; kk < kKpt; ++kk) den = __fadd_rn(den, expf(__fsub_rn(z[kk][c], m)));
+        for (int kk = 0; kk < kKpt; ++kk) den = __fadd_rn(den, softmax_exp(__fsub_rn(z[kk][c], m)));
       }
       mloc[c] = m;
       dloc[c] = den;
@@ -327,7 +339,7 @@ bwd_chunk_kernel(const BwdParams bp) {
       float den = 0.0f;
       for (int y = 0; y < TY; ++y)
         den = __fadd_rn(den, __fmul_rn(d_s[y * tile_cols + cc],
-                                       expf(__fsub_rn(m_s[y * tile_cols + cc], M))));
+                                       softmax_exp(__fsub_rn(m_s[y * tile_cols + cc], M))));
       M_s[cc] = M;
       D_s[cc] = den;
     }
@@ -345,7 +357,7 @@ bwd_chunk_kernel(const BwdParams bp) {
       float s = 0.0f;
 #pragma unroll
       for (int kk = 0; kk < kKpt; ++kk) {
-        pk[kk][c] = __fdiv_rn(expf(__fsub_rn(z[kk][c], M)), D);
+        pk[kk][c] = __fdiv_rn(softmax_exp(__fsub_rn(z[kk][c], M)), D);
         const float x = bf16_at(c < 2 ? kvv[kk].x : kvv[kk].y, c & 1);
         s = __fadd_rn(s, __fmul_rn(__fmul_rn(g, x), pk[kk][c]));
       }
@@ -471,11 +483,11 @@ int occupancy(K kernel, int threads, size_t smem) {
 template <int R, int COFF>
 cudaError_t plan_small(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
-  const int nvec = p.d / kVec;
-  const int tx = nvec <= 128 ? nvec : 128;
+  const int ncv = p.d / kCv;
+  const int tx = ncv <= 128 ? ncv : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
-  const int tiles = (nvec + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kVec;
+  const int tiles = (ncv + tx - 1) / tx;
+  const size_t smem = sizeof(float) * W * tx * kCv;
   auto kern = bwd_small_kernel<R, COFF>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);

@@ -42,6 +42,36 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
+// ---- exp --------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2_approx_ftz(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+
+// exp(x) for the softmax weights, x = z - max <= 0 (or NaN).
+// exp(x) = 2^(x * log2 e). The product x * log2 e is carried beyond fp32
+// precision as t + err: log2 e is split into an fp32 head and tail, and the
+// head product's rounding error is recovered exactly with one FMA (the
+// TwoProduct step of Ogita, Rump & Oishi, "Accurate sum and dot product",
+// SIAM J. Sci. Comput. 26(6), 2005). Then 2^(t + err) = 2^t * (1 + err ln 2)
+// to first order (|err| <= 2^-17 here, so the dropped term is below 2^-35),
+// with 2^t from the hardware ex2.approx. x is clamped at -100 (exp(-100) is
+// below the smallest fp32 subnormal; ftz flushes results below 2^-126 to 0)
+// with a NaN-propagating max, so -inf gives 0 and NaN stays NaN.
+__device__ __forceinline__ float softmax_exp(float x) {
+  const float kLog2eHi = __int_as_float(0x3fb8aa3b);  // fp32(log2 e)
+  const float kLog2eLo = __int_as_float(0x32a57060);  // log2 e - kLog2eHi
+  const float kLn2 = __int_as_float(0x3f317218);      // fp32(ln 2)
+  x = max_nan(x, -100.0f);
+  const float t = __fmul_rn(x, kLog2eHi);
+  float err = __fmaf_rn(x, kLog2eHi, -t);
+  err = __fmaf_rn(x, kLog2eLo, err);
+  const float r = ex2_approx_ftz(t);
+  return __fmaf_rn(r, __fmul_rn(err, kLn2), r);
+}
+
 // ---- memory ----------------------------------------------------------------
 
 // kv / score / grad_out are read exactly once: streaming (evict-first) loads.
@@ -86,6 +116,42 @@ __device__ __forceinline__ RowInfo row_info(const int32_t* __restrict__ cu,
   }
   const int64_t c0 = __ldg(cuc + lo);
   const int64_t c1 = __ldg(cuc + lo + 1);
+  const int64_t i = b - c0;
+  ri.base = (int64_t)__ldg(cu + lo) + i * ratio;
+  ri.seg_end = __ldg(cu + lo + 1);
+  ri.first = (i == 0);
+  ri.last = (i == c1 - c0 - 1);
+  return ri;
+}
+
+// Same map for a thread that visits rows in increasing order: `hint` is a
+// segment with cu_seqlens_comp[hint] <= b from an earlier row (0 at first);
+// the common case costs one load.
+__device__ __forceinline__ RowInfo row_info_from(const int32_t* __restrict__ cu,
+                                                 const int32_t* __restrict__ cuc, int nseq,
+                                                 int64_t b, int64_t true_rows, int ratio,
+                                                 int& hint) {
+  RowInfo ri;
+  if (b >= true_rows) {
+    ri.base = 0;
+    ri.seg_end = 0;
+    ri.first = true;
+    ri.last = false;
+    return ri;
+  }
+  int lo = hint;
+  int64_t c1 = __ldg(cuc + lo + 1);
+  if (c1 <= b) {
+    int hi = nseq;
+    lo = lo + 1;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)__ldg(cuc + mid) <= b) lo = mid; else hi = mid;
+    }
+    c1 = __ldg(cuc + lo + 1);
+  }
+  hint = lo;
+  const int64_t c0 = __ldg(cuc + lo);
   const int64_t i = b - c0;
   ri.base = (int64_t)__ldg(cu + lo) + i * ratio;
   ri.seg_end = __ldg(cu + lo + 1);

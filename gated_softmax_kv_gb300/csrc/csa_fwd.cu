@@ -39,30 +39,36 @@ constexpr int kThreads = 256;
 constexpr int kKpt = 8;  // window slots per thread in the chunked kernels
 
 template <int R, int COFF>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 fwd_small_kernel(const FwdParams f) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
+  const int TX = blockDim.x, TY = blockDim.y;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx, nthr = TX * TY;
   const int nvec = p.d / kVec;
-  const int jv = blockIdx.x * blockDim.x + threadIdx.x;
-  if (jv >= nvec) return;  // no barrier in this kernel
+  const int jv = blockIdx.x * TX + tx;
   const int64_t ld = (int64_t)COFF * p.d;
   const int j0 = jv * kVec;
+  const int tile_cols = TX * kVec;
 
-  float apev[W][kVec];
-#pragma unroll
-  for (int k = 0; k < W; ++k) {
-    const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
-    const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
-    apev[k][0] = lo.x; apev[k][1] = lo.y; apev[k][2] = lo.z; apev[k][3] = lo.w;
-    apev[k][4] = hi.x; apev[k][5] = hi.y; apev[k][6] = hi.z; apev[k][7] = hi.w;
+  // APE slice of this column tile, [W][tile_cols], read once per CTA
+  extern __shared__ float sm[];
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    sm[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
   }
+  __syncthreads();
+  if (jv >= nvec) return;  // no barrier below
+  const float* ape_s = sm + tx * kVec;
 
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  const int64_t stride = (int64_t)gridDim.y * blockDim.y;
-  for (int64_t b = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; b < p.C; b += stride) {
-    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+  const int64_t stride = (int64_t)gridDim.y * TY;
+  int hint = 0;
+  for (int64_t b = (int64_t)blockIdx.y * TY + ty; b < p.C; b += stride) {
+    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     uint16_t* dst = f.out + b * p.d + j0;
     if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
       st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
@@ -80,6 +86,22 @@ fwd_small_kernel(const FwdParams f) {
         scv[k] = ld_stream(p.score + off);
       }
     }
+    // logits z = score + ape
+    float z[W][kVec];
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
+      const float4 a1 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols + 4);
+      z[k][0] = __fadd_rn(bf16_lo(scv[k].x), a0.x);
+      z[k][1] = __fadd_rn(bf16_hi(scv[k].x), a0.y);
+      z[k][2] = __fadd_rn(bf16_lo(scv[k].y), a0.z);
+      z[k][3] = __fadd_rn(bf16_hi(scv[k].y), a0.w);
+      z[k][4] = __fadd_rn(bf16_lo(scv[k].z), a1.x);
+      z[k][5] = __fadd_rn(bf16_hi(scv[k].z), a1.y);
+      z[k][6] = __fadd_rn(bf16_lo(scv[k].w), a1.z);
+      z[k][7] = __fadd_rn(bf16_hi(scv[k].w), a1.w);
+    }
+    // m = max z, e = exp(z - m), den = sum e, out = (sum e * kv) / den
     uint32_t ow[4];
 #pragma unroll
     for (int c2 = 0; c2 < 4; ++c2) {
@@ -87,24 +109,17 @@ fwd_small_kernel(const FwdParams f) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = 2 * c2 + h;
-        float z[W];
+        float m = z[0][c];
 #pragma unroll
-        for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), apev[k][c]);
-        float m = z[0];
-#pragma unroll
-        for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
-        float e[W];
-        float den = 0.0f;
+        for (int k = 1; k < W; ++k) m = max_nan(m, z[k][c]);
+        float den = 0.0f, acc = 0.0f;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          e[k] = expf(__fsub_rn(z[k], m));
-          den = __fadd_rn(den, e[k]);
+          const float e = softmax_exp(__fsub_rn(z[k][c], m));
+          den = __fadd_rn(den, e);
+          acc = __fmaf_rn(e, bf16_elem(kvv[k], c), acc);
         }
-        float acc = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k)
-          acc = __fadd_rn(acc, __fmul_rn(__fdiv_rn(e[k], den), bf16_elem(kvv[k], c)));
-        res[h] = acc;
+        res[h] = __fdiv_rn(acc, den);
       }
       ow[c2] = pack_bf16x2(res[0], res[1]);
     }
@@ -185,7 +200,7 @@ fwd_chunk_kernel(const FwdParams f) {
         if (m != -__int_as_float(0x7f800000)) {  // an all -inf chunk contributes nothing
 #pragma unroll
           for (int kk = 0; kk < kKpt; ++kk) {
-            const float e = expf(__fsub_rn(z[kk], m));
+            const float e = softmax_exp(__fsub_rn(z[kk], m));
             den = __fadd_rn(den, e);
             acc = __fadd_rn(acc, __fmul_rn(e, bf16_elem(kvv[kk], c)));
           }
@@ -219,7 +234,7 @@ fwd_chunk_kernel(const FwdParams f) {
         for (int y = 1; y < TY; ++y) M = max_nan(M, bm[y * tile_cols + cc + h]);
         float den = 0.0f, acc = 0.0f;
         for (int y = 0; y < TY; ++y) {
-          const float s = expf(__fsub_rn(bm[y * tile_cols + cc + h], M));
+          const float s = softmax_exp(__fsub_rn(bm[y * tile_cols + cc + h], M));
           den = __fadd_rn(den, __fmul_rn(bd[y * tile_cols + cc + h], s));
           acc = __fadd_rn(acc, __fmul_rn(ba[y * tile_cols + cc + h], s));
         }
@@ -247,14 +262,21 @@ cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
   const int tx = nvec <= 128 ? nvec : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (nvec + tx - 1) / tx;
+  constexpr int W = COFF * R;
+  const size_t smem = sizeof(float) * W * tx * kVec;
   auto kern = fwd_small_kernel<R, COFF>;
-  static int occ = occupancy(kern, tx * ty, 0);
+  static bool attr = [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    return true;
+  }();
+  (void)attr;
+  const int occ = occupancy(kern, tx * ty, smem);
   const int64_t row_blocks = (f.p.C + ty - 1) / ty;
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy < 1) gy = 1;
   if (gy > row_blocks) gy = row_blocks;
   if (gy > 65535) gy = 65535;
-  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, ty), 0, stream>>>(f);
+  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream>>>(f);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,5 @@
-"""Build the CUDA library (libcsa_compress.so) for sm_103a, in-tree.
+"""Build the CUDA library (libcsa_compress.so) for sm_103a, in-tree, plus the
+small libcsa_selftest.so that exposes device helpers to the GPU tests.
 
 Each translation unit under csrc/ is compiled by its own nvcc process (in
 parallel), then linked into gated_softmax_kv_gb300/_build/libcsa_compress.so
@@ -19,6 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libcsa_compress.so")
+SELFTEST_SRC = os.path.join(CSRC, "selftest", "csa_selftest.cu")
+SELFTEST_LIB = os.path.join(BUILD, "libcsa_selftest.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,13 +43,13 @@ def sources():
 
 def _inputs():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
+        glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__), SELFTEST_SRC]
 
 
 def stale() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(SELFTEST_LIB)):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(SELFTEST_LIB))
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
@@ -66,6 +69,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
             procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
                                                 text=True)))
+        st_tmp = SELFTEST_LIB + f".tmp{os.getpid()}"
+        cmd = [cc, *ARCH, *NVCC_FLAGS, "-shared", SELFTEST_SRC, "-o", st_tmp]
+        procs.append((SELFTEST_SRC, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                     stderr=subprocess.STDOUT, text=True)))
         failed = []
         for src, pr in procs:
             out, _ = pr.communicate()
@@ -78,6 +85,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         tmp = LIB + f".tmp{os.getpid()}"
         subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], check=True)
         os.replace(tmp, LIB)
+        os.replace(st_tmp, SELFTEST_LIB)
         return LIB
 
 

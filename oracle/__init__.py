@@ -70,6 +70,8 @@ def _load():
     i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.oracle_exp_f32.argtypes = [ctypes.c_float]
     lib.oracle_exp_f32.restype = ctypes.c_float
+    lib.oracle_exp_f32_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    lib.oracle_exp_f32_n.restype = None
     lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_mul_add_f32.argtypes = [ctypes.c_float] * 3
@@ -132,6 +134,13 @@ def validate(p: Problem) -> int:
 
 def exp_f32(x: float) -> float:
     return _load().oracle_exp_f32(x)
+
+
+def exp_f32_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    _load().oracle_exp_f32_n(_ptr(x), _ptr(y), x.size)
+    return y
 
 
 def f32_to_bf16(x: float) -> int:

@@ -97,6 +97,10 @@ extern "C" {
 
 float oracle_exp_f32(float x) { return (float)std::exp((double)x); }
 
+void oracle_exp_f32_n(const float* x, float* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = oracle_exp_f32(x[i]);
+}
+
 uint16_t oracle_f32_to_bf16(float x) {
   if (std::isnan(x)) return 0x7FC0;
   uint32_t u;

@@ -63,6 +63,7 @@ void oracle_window_slot(int32_t ratio, int32_t coff, int32_t head_dim,
 
 /* Correctly rounded fp32 exp used by O32 (exposed for its pin). */
 float oracle_exp_f32(float x);
+void oracle_exp_f32_n(const float* x, float* y, int64_t n);
 /* fp32 -> bf16 round-to-nearest-even, NaN -> 0x7FC0 (exposed for its pin). */
 uint16_t oracle_f32_to_bf16(float x);
 /* a*b + c as the oracle's translation unit evaluates it: two roundings, no FMA

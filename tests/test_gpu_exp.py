@@ -1,0 +1,53 @@
+"""Accuracy of the kernels' softmax exp against the oracle's correctly rounded
+fp32 exp, on the argument range the softmax produces (x = z - max <= 0)."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+def _ulp_dist(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    ia = a.view(np.int32).astype(np.int64)
+    ib = b.view(np.int32).astype(np.int64)
+    return np.abs(ia - ib)
+
+
+def test_softmax_exp_within_two_ulp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    lib.csa_selftest_softmax_exp.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_void_p]
+    lib.csa_selftest_softmax_exp.restype = ctypes.c_int32
+    # every 64th fp32 bit pattern in [-87, 0], plus dense samples near 0 and the specials
+    lo, hi = np.float32(-87.0).view(np.uint32), np.uint32(0x80000000)
+    xs = np.arange(hi, lo, 64, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    xs = np.concatenate([xs, np.linspace(-1.0, 0.0, 1 << 20, dtype=np.float32),
+                         np.array([0.0, -0.0, -1e-30, -87.3, -88.0, -100.0, -1e4], np.float32)])
+    x_d = torch.from_numpy(xs).cuda()
+    y_d = torch.empty_like(x_d)
+    assert lib.csa_selftest_softmax_exp(x_d.data_ptr(), y_d.data_ptr(), xs.size, None) == 0
+    torch.cuda.synchronize()
+    got = y_d.cpu().numpy()
+    want = oracle.exp_f32_array(xs)
+    normal = want >= np.float32(2.0 ** -126)
+    ulp = _ulp_dist(got[normal], want[normal])
+    print("max ulp", int(ulp.max()), "exact fraction", float(np.mean(ulp == 0)))
+    assert int(ulp.max()) <= 2
+    # results below the normal range are flushed to zero (or exact)
+    assert np.all(got[~normal] <= np.float32(2.0 ** -126))
+    # special inputs
+    sp = torch.tensor([float("-inf"), float("nan")], device="cuda")
+    out = torch.empty_like(sp)
+    assert lib.csa_selftest_softmax_exp(sp.data_ptr(), out.data_ptr(), 2, None) == 0
+    o = out.cpu().numpy()
+    assert o[0] == 0.0 and np.isnan(o[1])
