@@ -16,7 +16,7 @@ from . import nvbuild as _build
 LIB_PATH = _build.LIB
 
 CSA_STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_ALIGN", 3: "CSA_ERR_UNSUPPORTED",
-              4: "CSA_ERR_RANGE", 5: "CSA_ERR_CUDA"}
+              4: "CSA_ERR_RANGE", 5: "CSA_ERR_CUDA", 6: "CSA_ERR_SCRATCH"}
 
 _lib = None
 
@@ -165,3 +165,30 @@ def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int,
                          grad_out.data_ptr(), dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(),
                          _stream_handle(stream, dev))
     return dkv, dscore, dape
+
+
+# ------------------------------------------------------------- no-allocation backward
+
+NOALLOC_SCRATCH_FLOATS = 4 * 1024 * 1024
+
+
+def csa_compress_bwd_noalloc_ptr(kv: int, score: int, ape: int, cu_seqlens: int,
+                                 cu_seqlens_comp: int, num_seqs: int, total_tokens: int,
+                                 capacity: int, ratio: int, coff: int, head_dim: int,
+                                 grad_out: int, dkv: int, dscore: int, dape: int,
+                                 stream: int = 0) -> None:
+    """csa_compress_bwd_noalloc on raw device pointers: the backward for callers
+    that cannot allocate device memory at call time. Its dape partials use the
+    library's fixed 16 MiB device buffer, shared by every call (calls that
+    overlap on the GPU race on it); raises CsaError(CSA_ERR_SCRATCH) when a
+    problem needs more than that."""
+    lib = load()
+    fn = lib.csa_compress_bwd_noalloc
+    if fn.argtypes is None:
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp]
+        fn.restype = ctypes.c_int
+    st = fn(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity, ratio,
+            coff, head_dim, grad_out, dkv, dscore, dape, stream)
+    if st != 0:
+        _raise(st)

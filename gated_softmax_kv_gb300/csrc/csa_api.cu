@@ -89,6 +89,29 @@ cudaError_t workspace_pool(cudaMemPool_t* out) {
 
 }  // namespace
 
+namespace csa {
+
+// Argument checks of the backward, for the allocation-free entry point
+// (csa_noalloc.cu); the same checks csa_compress_bwd makes.
+csa_status_t check_bwd_args(const void* kv, const void* score, const float* ape, const int32_t* cu,
+                            const int32_t* cuc, int32_t num_seqs, int64_t total_tokens,
+                            int64_t capacity, int32_t ratio, int32_t coff, int32_t head_dim,
+                            const void* grad_out, const void* dkv, const void* dscore,
+                            const float* dape) {
+  csa_status_t st = validate(kv, score, ape, cu, cuc, num_seqs, total_tokens, capacity, ratio,
+                             coff, head_dim);
+  if (st != CSA_OK) return st;
+  if ((capacity > 0 && !grad_out) || (total_tokens > 0 && (!dkv || !dscore)) || !dape)
+    return CSA_ERR_NULL;
+  if (!aligned(grad_out, 16) || !aligned(dkv, 16) || !aligned(dscore, 16) || !aligned(dape, 16))
+    return CSA_ERR_ALIGN;
+  return CSA_OK;
+}
+
+csa_status_t record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+}  // namespace csa
+
 extern "C" {
 
 csa_status_t csa_compress_fwd(const void* kv, const void* score, const float* ape,
@@ -160,6 +183,7 @@ const char* csa_status_string(csa_status_t status) {
     case CSA_ERR_UNSUPPORTED: return "ratio, coff or head_dim outside the supported envelope";
     case CSA_ERR_RANGE: return "a size is negative, overflows int32 flat offsets, or capacity > 0 with total_tokens < ratio";
     case CSA_ERR_CUDA: return "a CUDA runtime call failed";
+    case CSA_ERR_SCRATCH: return "the backward needs more dape scratch than the no-allocation buffer holds (CSA_NOALLOC_SCRATCH_FLOATS)";
     default: return "unknown status";
   }
 }

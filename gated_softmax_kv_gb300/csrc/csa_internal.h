@@ -58,3 +58,18 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
 int sm_count();
 
 }  // namespace csa
+
+#include "csa_compress.h"
+
+namespace csa {
+
+// Backward argument checks shared with the allocation-free entry point, and
+// the per-thread record behind csa_last_cuda_error() (csa_api.cu).
+csa_status_t check_bwd_args(const void* kv, const void* score, const float* ape, const int32_t* cu,
+                            const int32_t* cuc, int32_t num_seqs, int64_t total_tokens,
+                            int64_t capacity, int32_t ratio, int32_t coff, int32_t head_dim,
+                            const void* grad_out, const void* dkv, const void* dscore,
+                            const float* dape);
+csa_status_t record_cuda_error(cudaError_t e);
+
+}  // namespace csa

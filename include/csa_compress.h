@@ -67,7 +67,9 @@ typedef enum csa_status {
   CSA_ERR_ALIGN = 2,       /* a base pointer is not aligned as required           */
   CSA_ERR_UNSUPPORTED = 3, /* ratio / coff / head_dim outside the envelope        */
   CSA_ERR_RANGE = 4,       /* a size is negative or overflows int32 flat offsets  */
-  CSA_ERR_CUDA = 5         /* a CUDA runtime call failed (see csa_last_cuda_error) */
+  CSA_ERR_CUDA = 5,        /* a CUDA runtime call failed (see csa_last_cuda_error) */
+  CSA_ERR_SCRATCH = 6      /* csa_compress_bwd_noalloc: the call needs more dape scratch
+                              than the library's fixed device buffer holds            */
 } csa_status_t;
 
 /*
@@ -104,6 +106,38 @@ csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ap
                               int32_t ratio, int32_t coff, int32_t head_dim,
                               const void* grad_out, void* dkv, void* dscore, float* dape,
                               cudaStream_t stream);
+
+/*
+ * Backward that allocates no device memory. This entry point has no
+ * counterpart in the paper; it exists for callers that cannot allocate device
+ * memory while they run the backward -- for example a process that hands all
+ * of its device memory to its own allocator at start-up, or a time-critical
+ * loop that must not enter the CUDA allocator (csa_compress_bwd takes its dape
+ * workspace from a stream-ordered memory pool, which can grow on first use).
+ *
+ * Same arguments, outputs and numerics as csa_compress_bwd (same kernels,
+ * same launch shape, so the results are bitwise identical). The dape partials
+ * live in one fixed array of CSA_NOALLOC_SCRATCH_FLOATS floats (16 MiB) that
+ * the library reserves statically on every GPU that loads it, for the life of
+ * the process. A call whose partials do not fit returns CSA_ERR_SCRATCH before
+ * launching anything (the headline and ratio-128 workloads of this repository
+ * need at most 2.6 Mi floats on a 152-SM GPU).
+ *
+ * The first call on a device looks up that array's device address (once per
+ * device, with the caller's device current); make that first call before any
+ * stream capture. All calls share the one array and leave their partials in
+ * it: calls whose kernels overlap on the GPU (different streams, or several
+ * host threads) race on it and must be serialised by the caller. Nothing in
+ * the array needs clearing between calls: each call overwrites every partial
+ * it reads.
+ */
+#define CSA_NOALLOC_SCRATCH_FLOATS (4 * 1024 * 1024)
+csa_status_t csa_compress_bwd_noalloc(const void* kv, const void* score, const float* ape,
+                                      const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                      int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                      int32_t ratio, int32_t coff, int32_t head_dim,
+                                      const void* grad_out, void* dkv, void* dscore, float* dape,
+                                      cudaStream_t stream);
 
 /* Static description of a status code (never null). */
 const char* csa_status_string(csa_status_t status);
