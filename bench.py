@@ -43,7 +43,17 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=262144,
                     help="scale the headline recipe to this many tokens (profiling runs)")
+    ap.add_argument("--workload", default="headline",
+                    choices=["headline", "r4d512", "r2d128rag", "r128c1"],
+                    help="another of the seeded workloads instead of the headline (profiling runs)")
     return ap.parse_args()
+
+
+def pick_case(args, seed: int, fill: bool = True):
+    import workloads
+    if args.workload == "headline":
+        return headline_case(args.tokens, seed=seed, fill=fill)
+    return workloads.config(args.workload, seed=seed, fill=fill)
 
 
 def headline_case(tokens: int, seed: int, fill: bool = True):
@@ -296,7 +306,7 @@ def run_gpu(args, rank, world, local):
 
     gsk.build()
     lib = gsk.load()  # noqa: F841  (fails loudly if the library is missing)
-    case = headline_case(args.tokens, seed=rank)
+    case = pick_case(args, seed=rank)
     T, C, r, coff, d = case.total_tokens, case.capacity, case.ratio, case.coff, case.head_dim
 
     def up(bits):
@@ -428,7 +438,8 @@ def run_gpu(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic (seeded SplitMix64/Box-Muller, the page's gate distribution)",
-        "config": {"workload": WORKLOAD if T == 262144 else f"headline recipe scaled to {T} tokens", "tokens": T, "true_rows": case.true_rows, "capacity": C,
+        "config": {"workload": (WORKLOAD if T == 262144 else f"headline recipe scaled to {T} tokens")
+                   if args.workload == "headline" else args.workload, "tokens": T, "true_rows": case.true_rows, "capacity": C,
                    "ratio": r, "coff": coff, "head_dim": d, "segments": case.num_seqs,
                    "l2": "inputs larger than L2 (kv+score 1 GiB per step), no flush",
                    "step": "csa_compress_fwd + csa_compress_bwd (3 kernels)"},

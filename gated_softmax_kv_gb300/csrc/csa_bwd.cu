@@ -74,28 +74,33 @@ __device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
 
 // Small window (W <= 8): blockDim = (TX, TY); a thread owns 4 consecutive
 // columns (8-byte vectors) of one row at a time, rows strided by the grid.
-template <int R, int COFF>
+// D > 0 fixes head_dim at compile time (slot offsets become immediates);
+// D == 0 reads it from the problem.
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_small_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = bp.p;
+  const int d = D > 0 ? D : p.d;
   const int TX = blockDim.x, TY = blockDim.y;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int tid = ty * TX + tx, nthr = TX * TY;
-  const int ncv = p.d / kCv;
+  const int ncv = d / kCv;
   const int cv = blockIdx.x * TX + tx;
   const bool col_ok = cv < ncv;
-  const int64_t ld = (int64_t)COFF * p.d;
+  const int64_t ld = (int64_t)COFF * d;
   const int j0 = cv * kCv;
   const int tile_cols = TX * kCv;
+  // element offset of slot k from (row base token, column j0)
+  auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
   // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    sm[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
+    sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
   __syncthreads();
   const float* ape_s = sm + tx * kCv;
@@ -113,90 +118,107 @@ bwd_small_kernel(const BwdParams bp) {
   for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
     const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
-    const bool has_grad = b < p.C;                    // rows past capacity have no output slot
-    uint2 kvv[W], scv[W];
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      if (S::masked(ri.first, k)) {
-        kvv[k] = zero2;
-        scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
-      } else {
-        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-        kvv[k] = ld_stream8(p.kv + off);
-        scv[k] = ld_stream8(p.score + off);
-      }
-    }
-    const uint2 gv = has_grad ? ld_stream8(bp.grad_out + b * p.d + j0) : zero2;
-
-    // z = score + ape, then in place e = exp(z - m), then p = e / den
-    float pz[W][kCv];
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
-      pz[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
-      pz[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
-      pz[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
-      pz[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
-    }
-    uint32_t dkw[W][2], dzw[W][2];
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      // both columns of the pair: m, e, den, p, then S
-      float sum[2], g[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 2 * c2 + h;
-        float m = pz[0][c];
-#pragma unroll
-        for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
-        float den = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          pz[k][c] = softmax_exp(__fsub_rn(pz[k][c], m));
-          den = __fadd_rn(den, pz[k][c]);
-        }
-#pragma unroll
-        for (int k = 0; k < W; ++k) pz[k][c] = __fdiv_rn(pz[k][c], den);
-        g[h] = has_grad ? bf16_at(c2 ? gv.y : gv.x, h) : 0.0f;
-        float acc = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
-          acc = __fadd_rn(acc, __fmul_rn(dp, pz[k][c]));
-        }
-        sum[h] = acc;
-      }
-      // dscore = p (dp - S), dkv = g p, packed per slot as soon as both columns exist
+    const int64_t rowoff = ri.base * ld + j0;
+    uint16_t* dkv_row = bp.dkv + rowoff;
+    uint16_t* dsc_row = bp.dscore + rowoff;
+    if (b < p.C) {
+      const uint16_t* kv_row = p.kv + rowoff;
+      const uint16_t* sc_row = p.score + rowoff;
+      uint2 kvv[W], scv[W];
 #pragma unroll
       for (int k = 0; k < W; ++k) {
-        float dz[2], dk[2];
+        if (S::masked(ri.first, k)) {
+          kvv[k] = zero2;
+          scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+        } else {
+          kvv[k] = ld_stream8(kv_row + koff(k));
+          scv[k] = ld_stream8(sc_row + koff(k));
+        }
+      }
+      const uint2 gv = ld_stream8(bp.grad_out + b * d + j0);
+
+      // z = score + ape, then in place e = exp(z - m), then p = e / den
+      float pz[W][kCv];
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
+        pz[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
+        pz[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
+        pz[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
+        pz[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
+      }
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        // both columns of the pair: m, e, den, p, then S
+        float sum[2], g[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = 2 * c2 + h;
-          const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
-          dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
-          dk[h] = __fmul_rn(g[h], pz[k][c]);
-          if (has_grad) dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);
-        }
-        dkw[k][c2] = has_grad ? pack_bf16x2(dk[0], dk[1]) : 0u;
-        dzw[k][c2] = has_grad ? pack_bf16x2(dz[0], dz[1]) : 0u;
-      }
-    }
+          float m = pz[0][c];
 #pragma unroll
-    for (int k = 0; k < W; ++k) {
-      if (S::masked(ri.first, k)) continue;
-      const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-      st_stream8(bp.dkv + off, make_uint2(dkw[k][0], dkw[k][1]));
-      st_stream8(bp.dscore + off, make_uint2(dzw[k][0], dzw[k][1]));
+          for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
+          float den = 0.0f;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            pz[k][c] = softmax_exp(__fsub_rn(pz[k][c], m));
+            den = __fadd_rn(den, pz[k][c]);
+          }
+          const float y = __frcp_rn(den);
+#pragma unroll
+          for (int k = 0; k < W; ++k) pz[k][c] = div_rn_by_rcp(pz[k][c], den, y);
+          g[h] = bf16_at(c2 ? gv.y : gv.x, h);
+          float acc = 0.0f;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+            acc = __fadd_rn(acc, __fmul_rn(dp, pz[k][c]));
+          }
+          sum[h] = acc;
+        }
+        // dscore = p (dp - S), dkv = g p, packed per slot as soon as both columns exist;
+        // the packed words reuse the raw score registers, which are dead by now
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          float dz[2], dk[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
+            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+            dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
+            dk[h] = __fmul_rn(g[h], pz[k][c]);
+            dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);
+          }
+          if (c2 == 0) {
+            scv[k].x = pack_bf16x2(dz[0], dz[1]);
+            kvv[k].x = pack_bf16x2(dk[0], dk[1]);
+          } else {
+            scv[k].y = pack_bf16x2(dz[0], dz[1]);
+            kvv[k].y = pack_bf16x2(dk[0], dk[1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        if (S::masked(ri.first, k)) continue;
+        st_stream8(dkv_row + koff(k), kvv[k]);
+        st_stream8(dsc_row + koff(k), scv[k]);
+      }
+    } else {
+      // a row past capacity has no output slot: zero gradient at its positions
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        if (S::masked(ri.first, k)) continue;
+        st_stream8(dkv_row + koff(k), zero2);
+        st_stream8(dsc_row + koff(k), zero2);
+      }
     }
     if (ri.last) {
       // the segment's last row owns its block's unread first-half columns ...
       if (COFF == 2) {
 #pragma unroll
         for (int t = 0; t < R; ++t) {
-          const int64_t off = (ri.base + t) * ld + j0;
-          st_stream8(bp.dkv + off, zero2);
-          st_stream8(bp.dscore + off, zero2);
+          st_stream8(dkv_row + t * ld, zero2);
+          st_stream8(dsc_row + t * ld, zero2);
         }
       }
       // ... and the segment's tail tokens (seqlen % ratio of them)
@@ -204,7 +226,7 @@ bwd_small_kernel(const BwdParams bp) {
       for (int64_t tok = ri.base + R; tok < tail_end; ++tok) {
 #pragma unroll
         for (int h = 0; h < COFF; ++h) {
-          const int64_t off = tok * ld + h * p.d + j0;
+          const int64_t off = tok * ld + h * d + j0;
           st_stream8(bp.dkv + off, zero2);
           st_stream8(bp.dscore + off, zero2);
         }
@@ -233,7 +255,7 @@ bwd_small_kernel(const BwdParams bp) {
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    if (col < p.d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col] = sm[i];
+    if (col < d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = sm[i];
   }
 }
 
@@ -480,15 +502,15 @@ int occupancy(K kernel, int threads, size_t smem) {
   return blocks;
 }
 
-template <int R, int COFF>
-cudaError_t plan_small(const Problem& p, BwdShape* s) {
+template <int R, int COFF, int D>
+cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
   const int ncv = p.d / kCv;
   const int tx = ncv <= 128 ? ncv : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (ncv + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kCv;
-  auto kern = bwd_small_kernel<R, COFF>;
+  auto kern = bwd_small_kernel<R, COFF, D>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
     return true;
@@ -505,6 +527,13 @@ cudaError_t plan_small(const Problem& p, BwdShape* s) {
   s->smem = smem;
   s->groups = (int32_t)gy;
   return cudaSuccess;
+}
+
+template <int R, int COFF>
+cudaError_t plan_small(const Problem& p, BwdShape* s) {
+  if (p.d == 512) return plan_small_d<R, COFF, 512>(p, s);
+  if (p.d == 128) return plan_small_d<R, COFF, 128>(p, s);
+  return plan_small_d<R, COFF, 0>(p, s);
 }
 
 template <int R, int COFF>
@@ -537,7 +566,12 @@ cudaError_t plan_chunk(const Problem& p, BwdShape* s) {
 
 template <int R, int COFF>
 cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  bwd_small_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
+  if (b.p.d == 512)
+    bwd_small_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
+  else if (b.p.d == 128)
+    bwd_small_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
+  else
+    bwd_small_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
   return cudaGetLastError();
 }
 

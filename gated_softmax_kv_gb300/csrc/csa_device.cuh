@@ -72,6 +72,24 @@ __device__ __forceinline__ float softmax_exp(float x) {
   return __fmaf_rn(r, __fmul_rn(err, kLn2), r);
 }
 
+// ---- division ---------------------------------------------------------------
+
+// a / b rounded to nearest from y = RN(1/b): q = RN(a*y), then one
+// correction step with the exact remainder r = a - b*q (an FMA computes it
+// exactly), q' = RN(q + r*y). With y the correctly rounded reciprocal this
+// returns the correctly rounded quotient when nothing overflows or
+// underflows (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the theorem is
+// restated in Muller et al., "Handbook of Floating-Point Arithmetic",
+// section on Newton-Raphson-based division with an FMA). The softmax uses it
+// with a = e in [0, 1] and b = den in [1, W], where one reciprocal per column
+// serves all W slots.
+__device__ __forceinline__ float div_rn_by_rcp(float a, float b, float y) {
+  const float q = __fmul_rn(a, y);
+  const float r = __fmaf_rn(-b, q, a);
+  return __fmaf_rn(r, y, q);
+}
+
 // ---- memory ----------------------------------------------------------------
 
 // kv / score / grad_out are read exactly once: streaming (evict-first) loads.

@@ -12,10 +12,11 @@
 //
 //  * fwd_small (window W = coff*ratio <= 8): a thread owns one output row and
 //    8 consecutive columns. It issues all 2W 16-byte loads of its window up
-//    front (one coalesced 512-byte request per warp per slot), keeps its APE
-//    columns in registers across the rows it visits (persistent grid, rows
-//    strided by the whole grid) and evaluates the plain eager order: m = max z,
-//    e = exp(z - m), den = sum e, p = e / den, out = sum p * kv.
+//    front (one coalesced 512-byte request per warp per slot), reads its APE
+//    columns from a shared-memory slice staged once per CTA (persistent grid,
+//    rows strided by the whole grid) and evaluates m = max z, e = exp(z - m),
+//    den = sum e in slot order and out = (sum e * kv) / den: one division per
+//    output instead of one per slot.
 //
 //  * fwd_chunk (W >= 16, e.g. ratio = 128): a CTA owns one row of a column
 //    tile per step; its threadIdx.y rows split the window into chunks of 8
@@ -38,27 +39,32 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kKpt = 8;  // window slots per thread in the chunked kernels
 
-template <int R, int COFF>
+// D > 0 fixes head_dim at compile time (slot offsets become immediates);
+// D == 0 reads it from the problem.
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_small_kernel(const FwdParams f) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
+  const int d = D > 0 ? D : p.d;
   const int TX = blockDim.x, TY = blockDim.y;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int tid = ty * TX + tx, nthr = TX * TY;
-  const int nvec = p.d / kVec;
+  const int nvec = d / kVec;
   const int jv = blockIdx.x * TX + tx;
-  const int64_t ld = (int64_t)COFF * p.d;
+  const int64_t ld = (int64_t)COFF * d;
   const int j0 = jv * kVec;
   const int tile_cols = TX * kVec;
+  // element offset of slot k from (row base token, column j0)
+  auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
   // APE slice of this column tile, [W][tile_cols], read once per CTA
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    sm[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
+    sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
   __syncthreads();
   if (jv >= nvec) return;  // no barrier below
@@ -69,11 +75,14 @@ fwd_small_kernel(const FwdParams f) {
   int hint = 0;
   for (int64_t b = (int64_t)blockIdx.y * TY + ty; b < p.C; b += stride) {
     const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
-    uint16_t* dst = f.out + b * p.d + j0;
+    uint16_t* dst = f.out + b * d + j0;
     if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
       st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
       continue;
     }
+    const int64_t rowoff = ri.base * ld + j0;
+    const uint16_t* kv_row = p.kv + rowoff;
+    const uint16_t* sc_row = p.score + rowoff;
     uint4 kvv[W], scv[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) {
@@ -81,9 +90,8 @@ fwd_small_kernel(const FwdParams f) {
         kvv[k] = make_uint4(0u, 0u, 0u, 0u);
         scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
       } else {
-        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-        kvv[k] = ld_stream(p.kv + off);
-        scv[k] = ld_stream(p.score + off);
+        kvv[k] = ld_stream(kv_row + koff(k));
+        scv[k] = ld_stream(sc_row + koff(k));
       }
     }
     // logits z = score + ape
@@ -256,15 +264,15 @@ int occupancy(K kernel, int threads, size_t smem) {
   return blocks;
 }
 
-template <int R, int COFF>
-cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
+template <int R, int COFF, int D>
+cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
+  constexpr int W = COFF * R;
   const int nvec = f.p.d / kVec;
   const int tx = nvec <= 128 ? nvec : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (nvec + tx - 1) / tx;
-  constexpr int W = COFF * R;
   const size_t smem = sizeof(float) * W * tx * kVec;
-  auto kern = fwd_small_kernel<R, COFF>;
+  auto kern = fwd_small_kernel<R, COFF, D>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
     return true;
@@ -278,6 +286,13 @@ cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
   if (gy > 65535) gy = 65535;
   kern<<<dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream>>>(f);
   return cudaGetLastError();
+}
+
+template <int R, int COFF>
+cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
+  if (f.p.d == 512) return launch_small_d<R, COFF, 512>(f, stream);
+  if (f.p.d == 128) return launch_small_d<R, COFF, 128>(f, stream);
+  return launch_small_d<R, COFF, 0>(f, stream);
 }
 
 template <int R, int COFF>

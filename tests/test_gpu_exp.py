@@ -51,3 +51,32 @@ def test_softmax_exp_within_two_ulp():
     assert lib.csa_selftest_softmax_exp(sp.data_ptr(), out.data_ptr(), 2, None) == 0
     o = out.cpu().numpy()
     assert o[0] == 0.0 and np.isnan(o[1])
+
+
+def test_division_from_reciprocal_is_correctly_rounded():
+    """The kernels' a / b from one correctly rounded reciprocal per column
+    (Markstein's correction step) against IEEE division, on the softmax range
+    a = e in [0, 1], b = den in [1, 256], plus random normal operands."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    lib.csa_selftest_div.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p]
+    lib.csa_selftest_div.restype = ctypes.c_int32
+    rng = np.random.default_rng(7)
+    n = 1 << 24
+    a = np.concatenate([rng.random(n, dtype=np.float32),
+                        (2.0 ** rng.uniform(-120, 0, n)).astype(np.float32),
+                        rng.uniform(-1e3, 1e3, n).astype(np.float32)])
+    b = np.concatenate([rng.uniform(1.0, 256.0, n).astype(np.float32),
+                        rng.uniform(1.0, 16.0, n).astype(np.float32),
+                        (2.0 ** rng.uniform(-60, 60, n)).astype(np.float32)])
+    a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    q_d = torch.empty_like(a_d)
+    assert lib.csa_selftest_div(a_d.data_ptr(), b_d.data_ptr(), q_d.data_ptr(), a.size, None) == 0
+    torch.cuda.synchronize()
+    got = q_d.cpu().numpy()
+    want = a / b  # numpy: IEEE fp32 division, correctly rounded
+    normal = np.abs(want) >= np.float32(2.0 ** -126)
+    assert np.array_equal(got[normal].view(np.uint32), want[normal].view(np.uint32))
