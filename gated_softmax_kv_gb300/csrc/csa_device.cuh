@@ -82,11 +82,11 @@ __device__ __forceinline__ float softmax_exp(float x) {
 // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the theorem is
 // restated in Muller et al., "Handbook of Floating-Point Arithmetic",
 // section on Newton-Raphson-based division with an FMA). The theorem needs
-// the remainder to be exact, which fails once it underflows: with b in
-// [1, 256] the quotient is correctly rounded for |a| >= 2^-110 (checked
-// exactly), and can be one ulp off below that. The softmax uses it with
-// a = e in [0, 1] and b = den in [1, W], where one reciprocal per column serves
-// all W slots; e < 2^-110 means a weight below 2^-110 of the row maximum.
+// the remainder to be exact: its last bit is ulp(b) * ulp(q), which stays in
+// fp32 range when the quotient is at least 2^-103 (b >= 1). Below that the
+// result can be one ulp off. The softmax uses it with a = e in [0, 1] and
+// b = den in [1, W], where one reciprocal per column serves all W slots; a
+// weight below 2^-103 is the only case outside the correctly rounded domain.
 __device__ __forceinline__ float div_rn_by_rcp(float a, float b, float y) {
   const float q = __fmul_rn(a, y);
   const float r = __fmaf_rn(-b, q, a);
