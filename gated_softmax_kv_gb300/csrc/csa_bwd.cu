@@ -32,15 +32,8 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKpt = 8;   // window slots per thread in the chunked kernel
 constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
 
-__device__ __forceinline__ uint2 ld_stream8(const uint16_t* p) {
-  return __ldcs(reinterpret_cast<const uint2*>(p));
-}
-__device__ __forceinline__ void st_stream8(uint16_t* p, uint2 v) {
-  __stcs(reinterpret_cast<uint2*>(p), v);
-}
 
 // Zeros for the positions no row reads that belong to nobody's window:
 // segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
@@ -259,215 +252,221 @@ bwd_small_kernel(const BwdParams bp) {
   }
 }
 
-// Chunked window: blockDim = (TX, TY), TY = W / kKpt; a thread owns 8 slots
-// x 4 columns; the CTA walks rows b = blockIdx.y, blockIdx.y + gridDim.y, ...
+// Long window (W >= 16): blockDim = (32, NCH) with NCH = W / KPT (KPT = 8
+// slots per warp, 16 for W = 256). Warp y owns window slots
+// [KPT y, KPT y + KPT) and lane l owns 2 consecutive columns (4-byte
+// vectors) of a 64-column tile (blockIdx.x), so every load and store of a
+// warp covers 128 contiguous bytes of one token row. The CTA walks rows
+// b = blockIdx.y, blockIdx.y + gridDim.y, ... and per row:
+//   phase 1  z = score + ape, the chunk's max and sum exp per column
+//   merge    (max, sum) of the NCH chunks of a column, in a fixed order:
+//            NCH/2 threads take 2 chunks each, then a butterfly over those
+//            lanes (commutative combines, so every lane gets the same bits)
+//   phase 2  p = exp(z - M) / den (one reciprocal per column), the chunk's
+//            share of S = sum (g kv) p
+//   merge    S the same way
+//   phase 3  dscore = p (g kv - S), dkv = g p, stores; dape accumulates in
+//            registers (each thread owns its KPT slots x 2 columns)
+constexpr int kLongVc = 2;   // columns per lane
+
+template <int W>
+struct LongShape {
+  static constexpr int kKpt = W >= 256 ? 16 : 8;  // slots per warp
+  static constexpr int kNch = W / kKpt;           // warps per CTA
+  static constexpr int kThreads = 32 * kNch;
+};
+
+// fixed-order merge of (max, sum exp) pairs: m = max, s = s_a e^(m_a - m) + s_b e^(m_b - m)
+__device__ __forceinline__ void merge_max_sum(float& m, float& s, float mb, float sb) {
+  const float kNegInf = __int_as_float(0xff800000);
+  const float mn = max_nan(m, mb);
+  const float mu = mn == kNegInf ? 0.0f : mn;
+  s = __fadd_rn(__fmul_rn(s, softmax_exp(__fsub_rn(m, mu))),
+                __fmul_rn(sb, softmax_exp(__fsub_rn(mb, mu))));
+  m = mn;
+}
+
 template <int R, int COFF>
-__global__ void __launch_bounds__(kThreads, 2)
-bwd_chunk_kernel(const BwdParams bp) {
+__global__ void __launch_bounds__(LongShape<COFF * R>::kThreads,
+                                  LongShape<COFF * R>::kThreads >= 512 ? 1 : 2)
+bwd_long_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
-  constexpr int TY = W / kKpt;
+  constexpr int kLongKpt = LongShape<W>::kKpt;
+  constexpr int NCH = LongShape<W>::kNch;
+  constexpr int NT = LongShape<W>::kThreads;
+  constexpr int TC = 32 * kLongVc;      // tile columns
+  constexpr int G = NCH / kLongVc;      // merge threads per column
+  constexpr int LDS = TC + 1;           // padded row stride of the chunk tables
   using S = Slot<R, COFF>;
   const Problem& p = bp.p;
-  const int TX = blockDim.x;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  const int tid = ty * TX + tx, nthr = TX * TY;
-  const int ncv = p.d / kCv;
-  const int cv = blockIdx.x * TX + tx;
+  const int d = p.d;
+  const int lane = threadIdx.x, y = threadIdx.y;
+  const int tid = y * 32 + lane;
+  const int ncv = d / kLongVc;
+  const int cv = blockIdx.x * 32 + lane;
   const bool col_ok = cv < ncv;
-  const int64_t ld = (int64_t)COFF * p.d;
-  const int j0 = cv * kCv;
-  const int k0 = ty * kKpt;
-  const int tile_cols = TX * kCv;
+  const int64_t ld = (int64_t)COFF * d;
+  const int j0 = cv * kLongVc;
+  const int k0 = y * kLongKpt;
   const float kNegInf = __int_as_float(0xff800000);
 
-  extern __shared__ float sm[];
-  float* ape_s = sm;                            // [W][tile_cols]
-  float* m_s = ape_s + W * tile_cols;           // [TY][tile_cols] chunk max
-  float* d_s = m_s + TY * tile_cols;            // [TY][tile_cols] chunk sum exp
-  float* s_s = d_s + TY * tile_cols;            // [TY][tile_cols] chunk S
-  float* M_s = s_s + TY * tile_cols;            // [tile_cols] merged max
-  float* D_s = M_s + tile_cols;                 // [tile_cols] merged den
-  float* S_s = D_s + tile_cols;                 // [tile_cols] merged S
+  __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
+  __shared__ float M_s[TC], D_s[TC], S_s[TC];
 
-  for (int i = tid; i < W * tile_cols; i += nthr) {
-    const int k = i / tile_cols;
-    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    ape_s[i] = col < p.d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + col) : 0.0f;
-  }
-  __syncthreads();
+  // this thread's APE values (slots k0.., columns j0, j0+1) are re-read per row through L1
+  const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
 
-  float dacc[kKpt][kCv];
+  float dacc[kLongKpt][kLongVc];
 #pragma unroll
-  for (int kk = 0; kk < kKpt; ++kk)
-#pragma unroll
-    for (int c = 0; c < kCv; ++c) dacc[kk][c] = 0.0f;
+  for (int t = 0; t < kLongKpt; ++t) dacc[t][0] = dacc[t][1] = 0.0f;
 
-  const uint2 zero2 = make_uint2(0u, 0u);
+  // merge thread layout: column mc of the tile, group member mq (G per column)
+  const int mc = tid / G, mq = tid % G;
+
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
   for (int64_t b = blockIdx.y; b < true_rows; b += gridDim.y) {
     const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
     if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // uniform over the CTA
-    const bool has_grad = b < p.C;
     const bool chunk_masked = S::masked(ri.first, k0);
     const bool active = col_ok && !chunk_masked;
-    const int64_t base_off = S::tok(ri.base, k0) * ld + S::half(k0) * p.d + j0;
-
-    // phase 1: chunk max and sum of exp
-    uint2 kvv[kKpt], scv[kKpt];
-    float mloc[kCv], dloc[kCv];
-    if (active) {
+    const int64_t off = ri.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
+    if (b < p.C) {
+      // phase 1
+      uint32_t kvw[kLongKpt], scw[kLongKpt];
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        kvv[kk] = ld_stream8(p.kv + base_off + kk * ld);
-        scv[kk] = ld_stream8(p.score + base_off + kk * ld);
+      for (int t = 0; t < kLongKpt; ++t) {
+        kvw[t] = active ? __ldcs(reinterpret_cast<const uint32_t*>(p.kv + off + t * ld)) : 0u;
+        scw[t] = active ? __ldcs(reinterpret_cast<const uint32_t*>(p.score + off + t * ld))
+                        : kNegInfBf16x2;
       }
-    } else {
+      const uint32_t gw = col_ok ? __ldcs(reinterpret_cast<const uint32_t*>(bp.grad_out + b * d + j0)) : 0u;
+      float pz[kLongKpt][kLongVc];
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        kvv[kk] = zero2;
-        scv[kk] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+      for (int t = 0; t < kLongKpt; ++t) {
+        const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld))
+                                : make_float2(0.0f, 0.0f);
+        pz[t][0] = __fadd_rn(bf16_lo(scw[t]), a.x);
+        pz[t][1] = __fadd_rn(bf16_hi(scw[t]), a.y);
       }
-    }
-    float z[kKpt][kCv];
 #pragma unroll
-    for (int c = 0; c < kCv; ++c) {
-      const uint32_t sh = c < 2 ? 0 : 1;
+      for (int c = 0; c < kLongVc; ++c) {
+        float m = pz[0][c];
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        const uint32_t w = sh ? scv[kk].y : scv[kk].x;
-        z[kk][c] = __fadd_rn(bf16_at(w, c & 1), ape_s[(k0 + kk) * tile_cols + tx * kCv + c]);
+        for (int t = 1; t < kLongKpt; ++t) m = max_nan(m, pz[t][c]);
+        float sum = 0.0f;
+        if (m != kNegInf) {  // an all -inf chunk contributes nothing
+#pragma unroll
+          for (int t = 0; t < kLongKpt; ++t) sum = __fadd_rn(sum, softmax_exp(__fsub_rn(pz[t][c], m)));
+        }
+        m_s[y * LDS + lane * kLongVc + c] = m;
+        d_s[y * LDS + lane * kLongVc + c] = sum;
       }
-      float m = z[0][c];
+      __syncthreads();
+      {
+        float m = m_s[(mq * kLongVc) * LDS + mc], sm = d_s[(mq * kLongVc) * LDS + mc];
 #pragma unroll
-      for (int kk = 1; kk < kKpt; ++kk) m = max_nan(m, z[kk][c]);
-      float den = 0.0f;
-      if (m != kNegInf) {
+        for (int i = 1; i < kLongVc; ++i)
+          merge_max_sum(m, sm, m_s[(mq * kLongVc + i) * LDS + mc], d_s[(mq * kLongVc + i) * LDS + mc]);
 #pragma unroll
-        for (int kk = 0; kk < kKpt; ++kk) den = __fadd_rn(den, softmax_exp(__fsub_rn(z[kk][c], m)));
-      }
-      mloc[c] = m;
-      dloc[c] = den;
-    }
-    {
-      float4* mw = reinterpret_cast<float4*>(m_s + ty * tile_cols + tx * kCv);
-      float4* dw = reinterpret_cast<float4*>(d_s + ty * tile_cols + tx * kCv);
-      *mw = make_float4(mloc[0], mloc[1], mloc[2], mloc[3]);
-      *dw = make_float4(dloc[0], dloc[1], dloc[2], dloc[3]);
-    }
-    __syncthreads();
-    for (int cc = tid; cc < tile_cols; cc += nthr) {
-      float M = m_s[cc];
-      for (int y = 1; y < TY; ++y) M = max_nan(M, m_s[y * tile_cols + cc]);
-      float den = 0.0f;
-      for (int y = 0; y < TY; ++y)
-        den = __fadd_rn(den, __fmul_rn(d_s[y * tile_cols + cc],
-                                       softmax_exp(__fsub_rn(m_s[y * tile_cols + cc], M))));
-      M_s[cc] = M;
-      D_s[cc] = den;
-    }
-    __syncthreads();
-
-    // phase 2: weights and the chunk's share of S
-    const uint2 gv = (has_grad && col_ok) ? ld_stream8(bp.grad_out + b * p.d + j0) : zero2;
-    float pk[kKpt][kCv];
-    float sloc[kCv];
-#pragma unroll
-    for (int c = 0; c < kCv; ++c) {
-      const float M = M_s[tx * kCv + c];
-      const float D = D_s[tx * kCv + c];
-      const float g = bf16_at(c < 2 ? gv.x : gv.y, c & 1);
-      float s = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        pk[kk][c] = __fdiv_rn(softmax_exp(__fsub_rn(z[kk][c], M)), D);
-        const float x = bf16_at(c < 2 ? kvv[kk].x : kvv[kk].y, c & 1);
-        s = __fadd_rn(s, __fmul_rn(__fmul_rn(g, x), pk[kk][c]));
-      }
-      sloc[c] = s;
-    }
-    *reinterpret_cast<float4*>(s_s + ty * tile_cols + tx * kCv) =
-        make_float4(sloc[0], sloc[1], sloc[2], sloc[3]);
-    __syncthreads();
-    for (int cc = tid; cc < tile_cols; cc += nthr) {
-      float s = 0.0f;
-      for (int y = 0; y < TY; ++y) s = __fadd_rn(s, s_s[y * tile_cols + cc]);
-      S_s[cc] = s;
-    }
-    __syncthreads();
-
-    // phase 3: gradients, stores, dape accumulation
-    uint32_t dkw[kKpt][2], dzw[kKpt][2];
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      float dk2[kKpt][2], dz2[kKpt][2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 2 * c2 + h;
-        const float sum = S_s[tx * kCv + c];
-        const float g = bf16_at(c2 ? gv.y : gv.x, h);
-#pragma unroll
-        for (int kk = 0; kk < kKpt; ++kk) {
-          const float x = bf16_at(c2 ? kvv[kk].y : kvv[kk].x, h);
-          const float dz = __fmul_rn(pk[kk][c], __fsub_rn(__fmul_rn(g, x), sum));
-          const float dk = __fmul_rn(g, pk[kk][c]);
-          dz2[kk][h] = has_grad ? dz : 0.0f;
-          dk2[kk][h] = has_grad ? dk : 0.0f;
-          if (has_grad) dacc[kk][c] = __fadd_rn(dacc[kk][c], dz);
+        for (int mask = 1; mask < G; mask <<= 1)
+          merge_max_sum(m, sm, __shfl_xor_sync(0xffffffffu, m, mask),
+                        __shfl_xor_sync(0xffffffffu, sm, mask));
+        if (mq == 0) {
+          M_s[mc] = m;
+          D_s[mc] = sm;
         }
       }
+      __syncthreads();
+      // phase 2
+      float g[kLongVc], ssum[kLongVc];
+      g[0] = bf16_lo(gw);
+      g[1] = bf16_hi(gw);
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        dkw[kk][c2] = pack_bf16x2(dk2[kk][0], dk2[kk][1]);
-        dzw[kk][c2] = pack_bf16x2(dz2[kk][0], dz2[kk][1]);
+      for (int c = 0; c < kLongVc; ++c) {
+        const float M = M_s[lane * kLongVc + c];
+        const float den = D_s[lane * kLongVc + c];
+        const float mu = M == kNegInf ? 0.0f : M;
+        const float yr = __frcp_rn(den);
+        float acc = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kLongKpt; ++t) {
+          pz[t][c] = div_rn_by_rcp(softmax_exp(__fsub_rn(pz[t][c], mu)), den, yr);
+          const float dp = __fmul_rn(g[c], bf16_at(kvw[t], c));
+          acc = __fadd_rn(acc, __fmul_rn(dp, pz[t][c]));
+        }
+        ssum[c] = acc;
+        s_s[y * LDS + lane * kLongVc + c] = acc;
       }
-    }
-    if (active) {
+      (void)ssum;
+      __syncthreads();
+      {
+        float sm = s_s[(mq * kLongVc) * LDS + mc];
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        st_stream8(bp.dkv + base_off + kk * ld, make_uint2(dkw[kk][0], dkw[kk][1]));
-        st_stream8(bp.dscore + base_off + kk * ld, make_uint2(dzw[kk][0], dzw[kk][1]));
+        for (int i = 1; i < kLongVc; ++i) sm = __fadd_rn(sm, s_s[(mq * kLongVc + i) * LDS + mc]);
+#pragma unroll
+        for (int mask = 1; mask < G; mask <<= 1) sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, mask));
+        if (mq == 0) S_s[mc] = sm;
+      }
+      __syncthreads();
+      // phase 3
+      const float S0 = S_s[lane * kLongVc], S1 = S_s[lane * kLongVc + 1];
+#pragma unroll
+      for (int t = 0; t < kLongKpt; ++t) {
+        const float dz0 = __fmul_rn(pz[t][0], __fsub_rn(__fmul_rn(g[0], bf16_lo(kvw[t])), S0));
+        const float dz1 = __fmul_rn(pz[t][1], __fsub_rn(__fmul_rn(g[1], bf16_hi(kvw[t])), S1));
+        dacc[t][0] = __fadd_rn(dacc[t][0], dz0);
+        dacc[t][1] = __fadd_rn(dacc[t][1], dz1);
+        if (active) {
+          __stcs(reinterpret_cast<uint32_t*>(bp.dkv + off + t * ld),
+                 pack_bf16x2(__fmul_rn(g[0], pz[t][0]), __fmul_rn(g[1], pz[t][1])));
+          __stcs(reinterpret_cast<uint32_t*>(bp.dscore + off + t * ld), pack_bf16x2(dz0, dz1));
+        }
+      }
+    } else if (active) {
+      // a row past capacity has no output slot: zero gradient at its positions
+#pragma unroll
+      for (int t = 0; t < kLongKpt; ++t) {
+        __stcs(reinterpret_cast<uint32_t*>(bp.dkv + off + t * ld), 0u);
+        __stcs(reinterpret_cast<uint32_t*>(bp.dscore + off + t * ld), 0u);
       }
     }
     if (ri.last) {
-      // unread positions owned by the segment's last row, for this column tile
-      const int tile_cv = TX;
+      // unread positions owned by the segment's last row, for this column tile:
+      // its block's first-half columns (coff 2) and the segment tail
       const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
-      const int64_t n_first = COFF == 2 ? (int64_t)R * tile_cv : 0;
-      const int64_t n_tail = (tail_end - (ri.base + R)) * COFF * tile_cv;
-      for (int64_t i = tid; i < n_first + n_tail; i += nthr) {
+      const int64_t n_first = COFF == 2 ? (int64_t)R * 32 : 0;
+      const int64_t n_tail = (tail_end - (ri.base + R)) * COFF * 32;
+      for (int64_t i = tid; i < n_first + n_tail; i += NT) {
         int64_t tok;
         int h, x;
         if (i < n_first) {
-          tok = ri.base + i / tile_cv;
+          tok = ri.base + i / 32;
           h = 0;
-          x = (int)(i % tile_cv);
+          x = (int)(i % 32);
         } else {
-          const int64_t t = i - n_first;
-          tok = ri.base + R + t / (COFF * tile_cv);
-          h = (int)((t / tile_cv) % COFF);
-          x = (int)(t % tile_cv);
+          const int64_t q = i - n_first;
+          tok = ri.base + R + q / (COFF * 32);
+          h = (int)((q / 32) % COFF);
+          x = (int)(q % 32);
         }
-        const int col_v = blockIdx.x * tile_cv + x;
+        const int col_v = blockIdx.x * 32 + x;
         if (col_v >= ncv) continue;
-        const int64_t off = tok * ld + h * p.d + col_v * kCv;
-        st_stream8(bp.dkv + off, zero2);
-        st_stream8(bp.dscore + off, zero2);
+        const int64_t o = tok * ld + h * d + col_v * kLongVc;
+        __stcs(reinterpret_cast<uint32_t*>(bp.dkv + o), 0u);
+        __stcs(reinterpret_cast<uint32_t*>(bp.dscore + o), 0u);
       }
     }
   }
 
   zero_orphans(bp, R);
 
-  // each (slot, column) of the tile belongs to exactly one thread: write the
-  // partial of row group blockIdx.y directly
+  // each (slot, column) of the tile belongs to exactly one thread
   if (col_ok) {
     float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
 #pragma unroll
-    for (int kk = 0; kk < kKpt; ++kk) {
-      const int k = k0 + kk;
-      float* dst = part + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
-      *reinterpret_cast<float4*>(dst) = make_float4(dacc[kk][0], dacc[kk][1], dacc[kk][2], dacc[kk][3]);
-    }
+    for (int t = 0; t < kLongKpt; ++t)
+      *reinterpret_cast<float2*>(part + (int64_t)S::ape_row(k0 + t) * ld + S::half(k0) * d + j0) =
+          make_float2(dacc[t][0], dacc[t][1]);
   }
 }
 
@@ -537,29 +536,25 @@ cudaError_t plan_small(const Problem& p, BwdShape* s) {
 }
 
 template <int R, int COFF>
-cudaError_t plan_chunk(const Problem& p, BwdShape* s) {
+cudaError_t plan_long(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
-  constexpr int TY = W / kKpt;
-  const int ncv = p.d / kCv;
-  int tx = kThreads / TY;
-  if (tx > ncv) tx = ncv;
-  const int tiles = (ncv + tx - 1) / tx;
-  const int tile_cols = tx * kCv;
-  const size_t smem = sizeof(float) * ((size_t)W * tile_cols + 3 * (size_t)TY * tile_cols + 3 * tile_cols);
-  auto kern = bwd_chunk_kernel<R, COFF>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
-    return true;
-  }();
-  (void)attr;
-  const int occ = occupancy(kern, tx * TY, smem);
+  constexpr int NT = LongShape<W>::kThreads;
+  const int ncv = p.d / kLongVc;
+  const int tiles = (ncv + 31) / 32;
+  auto kern = bwd_long_kernel<R, COFF>;
+  const int occ = occupancy(kern, NT, 0);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy > p.C) gy = p.C;
   if (gy < 1) gy = 1;
+  // even out the rows per CTA
+  if (p.C > 0) {
+    const int64_t passes = (p.C + gy - 1) / gy;
+    gy = (p.C + passes - 1) / passes;
+  }
   if (gy > 65535) gy = 65535;
   s->grid = dim3(tiles, (unsigned)gy);
-  s->block = dim3(tx, TY);
-  s->smem = smem;
+  s->block = dim3(32, LongShape<W>::kNch);
+  s->smem = 0;
   s->groups = (int32_t)gy;
   return cudaSuccess;
 }
@@ -576,39 +571,39 @@ cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream
 }
 
 template <int R, int COFF>
-cudaError_t run_chunk(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  bwd_chunk_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
+cudaError_t run_long(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
+  bwd_long_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
   return cudaGetLastError();
 }
 
-#define CSA_BWD_DISPATCH(FN_SMALL, FN_CHUNK, ...)                 \
+#define CSA_BWD_DISPATCH(FN_SMALL, FN_LONG, ...)                 \
   switch (p.ratio * 4 + p.coff) {                                 \
     case 2 * 4 + 1: return FN_SMALL<2, 1>(__VA_ARGS__);           \
     case 2 * 4 + 2: return FN_SMALL<2, 2>(__VA_ARGS__);           \
     case 4 * 4 + 1: return FN_SMALL<4, 1>(__VA_ARGS__);           \
     case 4 * 4 + 2: return FN_SMALL<4, 2>(__VA_ARGS__);           \
     case 8 * 4 + 1: return FN_SMALL<8, 1>(__VA_ARGS__);           \
-    case 8 * 4 + 2: return FN_CHUNK<8, 2>(__VA_ARGS__);           \
-    case 16 * 4 + 1: return FN_CHUNK<16, 1>(__VA_ARGS__);         \
-    case 16 * 4 + 2: return FN_CHUNK<16, 2>(__VA_ARGS__);         \
-    case 32 * 4 + 1: return FN_CHUNK<32, 1>(__VA_ARGS__);         \
-    case 32 * 4 + 2: return FN_CHUNK<32, 2>(__VA_ARGS__);         \
-    case 64 * 4 + 1: return FN_CHUNK<64, 1>(__VA_ARGS__);         \
-    case 64 * 4 + 2: return FN_CHUNK<64, 2>(__VA_ARGS__);         \
-    case 128 * 4 + 1: return FN_CHUNK<128, 1>(__VA_ARGS__);       \
-    case 128 * 4 + 2: return FN_CHUNK<128, 2>(__VA_ARGS__);       \
+    case 8 * 4 + 2: return FN_LONG<8, 2>(__VA_ARGS__);           \
+    case 16 * 4 + 1: return FN_LONG<16, 1>(__VA_ARGS__);         \
+    case 16 * 4 + 2: return FN_LONG<16, 2>(__VA_ARGS__);         \
+    case 32 * 4 + 1: return FN_LONG<32, 1>(__VA_ARGS__);         \
+    case 32 * 4 + 2: return FN_LONG<32, 2>(__VA_ARGS__);         \
+    case 64 * 4 + 1: return FN_LONG<64, 1>(__VA_ARGS__);         \
+    case 64 * 4 + 2: return FN_LONG<64, 2>(__VA_ARGS__);         \
+    case 128 * 4 + 1: return FN_LONG<128, 1>(__VA_ARGS__);       \
+    case 128 * 4 + 2: return FN_LONG<128, 2>(__VA_ARGS__);       \
     default: return cudaErrorInvalidValue;                        \
   }
 
 }  // namespace
 
 cudaError_t plan_bwd(const Problem& p, BwdShape* shape) {
-  CSA_BWD_DISPATCH(plan_small, plan_chunk, p, shape)
+  CSA_BWD_DISPATCH(plan_small, plan_long, p, shape)
 }
 
 cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
   const Problem& p = b.p;
-  CSA_BWD_DISPATCH(run_small, run_chunk, b, shape, stream)
+  CSA_BWD_DISPATCH(run_small, run_long, b, shape, stream)
 }
 
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,

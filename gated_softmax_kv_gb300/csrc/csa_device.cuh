@@ -102,6 +102,12 @@ __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
 __device__ __forceinline__ void st_stream(uint16_t* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
+__device__ __forceinline__ uint2 ld_stream8(const uint16_t* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ void st_stream8(uint16_t* p, uint2 v) {
+  __stcs(reinterpret_cast<uint2*>(p), v);
+}
 __device__ __forceinline__ float4 ld_f4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
 }

@@ -18,12 +18,11 @@
 //    den = sum e in slot order and out = (sum e * kv) / den: one division per
 //    output instead of one per slot.
 //
-//  * fwd_chunk (W >= 16, e.g. ratio = 128): a CTA owns one row of a column
-//    tile per step; its threadIdx.y rows split the window into chunks of 8
-//    slots. Each thread reduces its chunk to a (max, sum exp, sum exp*kv)
-//    triple per column, and the triples are merged in a fixed chunk order in
-//    shared memory (double-buffered: one barrier per row). Deterministic; the
-//    merge reorders the sums, as the page's ratio = 128 kernels do.
+//  * fwd_long (W >= 16, e.g. ratio = 128): a thread owns one row and 4
+//    columns and streams the whole window in batches of 8 slots with an
+//    online softmax (running max, rescaled den and sum), prefetching the next
+//    batch. Deterministic; the rescaling reorders the sums, as the page's
+//    ratio = 128 kernels do.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,7 +36,6 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKpt = 8;  // window slots per thread in the chunked kernels
 
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
 // D == 0 reads it from the problem.
@@ -135,123 +133,114 @@ fwd_small_kernel(const FwdParams f) {
   }
 }
 
-// Chunked window: blockDim = (TX, TY), TY = W / kKpt chunks of 8 slots.
+// Long window (W >= 16): blockDim = (32, kLongRows). A lane owns 4
+// consecutive columns (8-byte vectors) of a 128-column tile (blockIdx.x) and
+// one row at a time (threadIdx.y, rows strided by the grid). It streams the
+// row's whole window in batches of 8 slots, prefetching the next batch while
+// it reduces the current one with an online softmax: running max m, and den
+// and acc rescaled by exp(m_old - m_new) whenever the max grows. No barriers,
+// no merges; consecutive lanes read consecutive 8-byte columns of the same
+// token row (256 bytes per warp per slot). The APE tile of the CTA (W slots x
+// 128 columns) is read through L1, where it stays for the rows the CTA visits.
+constexpr int kLongRows = 8;  // rows (warps) per CTA
+constexpr int kBatch = 8;     // window slots per batch
+
 template <int R, int COFF>
-__global__ void __launch_bounds__(kThreads)
-fwd_chunk_kernel(const FwdParams f) {
+__global__ void __launch_bounds__(32 * kLongRows, 2)
+fwd_long_kernel(const FwdParams f) {
   constexpr int W = COFF * R;
-  constexpr int TY = W / kKpt;
+  constexpr int NB = W / kBatch;  // even for every W >= 16
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
-  const int TX = blockDim.x;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  const int tid = ty * TX + tx;
-  const int nvec = p.d / kVec;
-  const int jv = blockIdx.x * TX + tx;
-  const bool col_ok = jv < nvec;
-  const int64_t ld = (int64_t)COFF * p.d;
-  const int j0 = jv * kVec;
-  const int k0 = ty * kKpt;
-  const int tile_cols = TX * kVec;
-
-  // [2 buffers][3 quantities][TY][tile_cols]
-  extern __shared__ float sm[];
-  const int qstride = TY * tile_cols;
-
-  float apev[kKpt][kVec];
-#pragma unroll
-  for (int kk = 0; kk < kKpt; ++kk) {
-    const int k = k0 + kk;
-    if (col_ok) {
-      const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * p.d + j0;
-      const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
-      apev[kk][0] = lo.x; apev[kk][1] = lo.y; apev[kk][2] = lo.z; apev[kk][3] = lo.w;
-      apev[kk][4] = hi.x; apev[kk][5] = hi.y; apev[kk][6] = hi.z; apev[kk][7] = hi.w;
-    } else {
-#pragma unroll
-      for (int c = 0; c < kVec; ++c) apev[kk][c] = 0.0f;
-    }
-  }
+  const int d = p.d;
+  const int ncv = d / 4;
+  const int cv = blockIdx.x * 32 + threadIdx.x;
+  if (cv >= ncv) return;  // no barrier in this kernel
+  const int64_t ld = (int64_t)COFF * d;
+  const int j0 = cv * 4;
+  const float kNegInf = __int_as_float(0xff800000);
+  const uint2 zero2 = make_uint2(0u, 0u);
+  const uint2 ninf2 = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
 
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  int buf = 0;
-  for (int64_t b = blockIdx.y; b < p.C; b += gridDim.y, buf ^= 1) {
-    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
-    const bool ok = row_in_bounds<R, COFF>(ri, p.T);
-    // chunk slots are all < R or all >= R (R is a multiple of 8): one mask test
-    const bool chunk_masked = S::masked(ri.first, k0);
-    float mloc[kVec], dloc[kVec], aloc[kVec];
-#pragma unroll
-    for (int c = 0; c < kVec; ++c) {
-      mloc[c] = -__int_as_float(0x7f800000);
-      dloc[c] = 0.0f;
-      aloc[c] = 0.0f;
+  const int64_t stride = (int64_t)gridDim.y * blockDim.y;
+  int hint = 0;
+  for (int64_t b = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; b < p.C; b += stride) {
+    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    uint16_t* dst = f.out + b * d + j0;
+    if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
+      st_stream8(dst, make_uint2(0x7FC07FC0u, 0x7FC07FC0u));
+      continue;
     }
-    if (col_ok && ok && !chunk_masked) {
-      uint4 kvv[kKpt], scv[kKpt];
+    const int64_t rowoff = ri.base * ld + j0;
+
+    // batch j: slots [8j, 8j+8), contiguous tokens, one half of the columns
+    auto load = [&](int j, uint2 (&kvb)[kBatch], uint2 (&scb)[kBatch]) {
+      const int k0 = j * kBatch;
+      if (S::masked(ri.first, k0)) {
 #pragma unroll
-      for (int kk = 0; kk < kKpt; ++kk) {
-        const int k = k0 + kk;
-        const int64_t off = S::tok(ri.base, k) * ld + S::half(k) * p.d + j0;
-        kvv[kk] = ld_stream(p.kv + off);
-        scv[kk] = ld_stream(p.score + off);
-      }
-#pragma unroll
-      for (int c = 0; c < kVec; ++c) {
-        float z[kKpt];
-#pragma unroll
-        for (int kk = 0; kk < kKpt; ++kk) z[kk] = __fadd_rn(bf16_elem(scv[kk], c), apev[kk][c]);
-        float m = z[0];
-#pragma unroll
-        for (int kk = 1; kk < kKpt; ++kk) m = max_nan(m, z[kk]);
-        float den = 0.0f, acc = 0.0f;
-        if (m != -__int_as_float(0x7f800000)) {  // an all -inf chunk contributes nothing
-#pragma unroll
-          for (int kk = 0; kk < kKpt; ++kk) {
-            const float e = softmax_exp(__fsub_rn(z[kk], m));
-            den = __fadd_rn(den, e);
-            acc = __fadd_rn(acc, __fmul_rn(e, bf16_elem(kvv[kk], c)));
-          }
+        for (int t = 0; t < kBatch; ++t) {
+          kvb[t] = zero2;
+          scb[t] = ninf2;
         }
-        mloc[c] = m;
-        dloc[c] = den;
-        aloc[c] = acc;
-      }
-    }
-    float* bm = sm + buf * 3 * qstride;
-    float* bd = bm + qstride;
-    float* ba = bd + qstride;
+      } else {
+        const int64_t off = rowoff + S::tok(0, k0) * ld + S::half(k0) * d;
 #pragma unroll
-    for (int c = 0; c < kVec; ++c) {
-      const int idx = ty * tile_cols + tx * kVec + c;
-      bm[idx] = mloc[c];
-      bd[idx] = dloc[c];
-      ba[idx] = aloc[c];
-    }
-    __syncthreads();
-    // merge the TY chunk triples of each column in ascending chunk order; a
-    // thread finishes two adjacent columns and stores one bf16x2 word
-    for (int pr = tid; pr < tile_cols / 2; pr += TX * TY) {
-      const int cc = 2 * pr;
-      const int col = blockIdx.x * tile_cols + cc;
-      if (col >= p.d) continue;
-      float res[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float M = bm[cc + h];
-        for (int y = 1; y < TY; ++y) M = max_nan(M, bm[y * tile_cols + cc + h]);
-        float den = 0.0f, acc = 0.0f;
-        for (int y = 0; y < TY; ++y) {
-          const float s = softmax_exp(__fsub_rn(bm[y * tile_cols + cc + h], M));
-          den = __fadd_rn(den, __fmul_rn(bd[y * tile_cols + cc + h], s));
-          acc = __fadd_rn(acc, __fmul_rn(ba[y * tile_cols + cc + h], s));
+        for (int t = 0; t < kBatch; ++t) {
+          kvb[t] = ld_stream8(p.kv + off + t * ld);
+          scb[t] = ld_stream8(p.score + off + t * ld);
         }
-        res[h] = __fdiv_rn(acc, den);
       }
-      uint32_t w = pack_bf16x2(res[0], res[1]);
-      if (!ok) w = 0x7FC07FC0u;
-      *reinterpret_cast<uint32_t*>(f.out + b * p.d + col) = w;
+    };
+    float m[4], den[4], acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      m[c] = kNegInf;
+      den[c] = 0.0f;
+      acc[c] = 0.0f;
     }
+    auto reduce = [&](int j, const uint2 (&kvb)[kBatch], const uint2 (&scb)[kBatch]) {
+      const int k0 = j * kBatch;
+      float z[kBatch][4];
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        const float4 a = ld_f4(p.ape + (int64_t)S::ape_row(k0 + t) * ld + S::half(k0) * d + j0);
+        z[t][0] = __fadd_rn(bf16_lo(scb[t].x), a.x);
+        z[t][1] = __fadd_rn(bf16_hi(scb[t].x), a.y);
+        z[t][2] = __fadd_rn(bf16_lo(scb[t].y), a.z);
+        z[t][3] = __fadd_rn(bf16_hi(scb[t].y), a.w);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float mn = m[c];
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) mn = max_nan(mn, z[t][c]);
+        // while every logit so far is -inf, shift by 0 so exp gives 0, not NaN
+        const float mu = mn == kNegInf ? 0.0f : mn;
+        const float alpha = softmax_exp(__fsub_rn(m[c], mu));
+        float dn = __fmul_rn(den[c], alpha);
+        float ac = __fmul_rn(acc[c], alpha);
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+          const float e = softmax_exp(__fsub_rn(z[t][c], mu));
+          dn = __fadd_rn(dn, e);
+          ac = __fmaf_rn(e, bf16_at(c < 2 ? kvb[t].x : kvb[t].y, c & 1), ac);
+        }
+        m[c] = mn;
+        den[c] = dn;
+        acc[c] = ac;
+      }
+    };
+    uint2 ka[kBatch], sa[kBatch], kb[kBatch], sb[kBatch];
+    load(0, ka, sa);
+    for (int j = 0; j < NB; j += 2) {
+      load(j + 1, kb, sb);
+      reduce(j, ka, sa);
+      if (j + 2 < NB) load(j + 2, ka, sa);
+      reduce(j + 1, kb, sb);
+    }
+    st_stream8(dst, make_uint2(pack_bf16x2(__fdiv_rn(acc[0], den[0]), __fdiv_rn(acc[1], den[1])),
+                               pack_bf16x2(__fdiv_rn(acc[2], den[2]), __fdiv_rn(acc[3], den[3]))));
   }
 }
 
@@ -296,26 +285,20 @@ cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
 }
 
 template <int R, int COFF>
-cudaError_t launch_chunk(const FwdParams& f, cudaStream_t stream) {
-  constexpr int W = COFF * R;
-  constexpr int TY = W / kKpt;
-  const int nvec = f.p.d / kVec;
-  int tx = kThreads / TY;
-  if (tx > nvec) tx = nvec;
-  const int tiles = (nvec + tx - 1) / tx;
-  const size_t smem = sizeof(float) * 2 * 3 * TY * tx * kVec;
-  auto kern = fwd_chunk_kernel<R, COFF>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    return true;
-  }();
-  (void)attr;
-  const int occ = occupancy(kern, tx * TY, smem);
+cudaError_t launch_long(const FwdParams& f, cudaStream_t stream) {
+  const int ncv = f.p.d / 4;
+  const int tiles = (ncv + 31) / 32;
+  auto kern = fwd_long_kernel<R, COFF>;
+  const int occ = occupancy(kern, 32 * kLongRows, 0);
+  const int64_t row_blocks = (f.p.C + kLongRows - 1) / kLongRows;
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy < 1) gy = 1;
-  if (gy > f.p.C) gy = f.p.C;
+  if (gy > row_blocks) gy = row_blocks;
+  // even out the rows per thread: the same number of passes for every CTA
+  const int64_t passes = (row_blocks + gy - 1) / gy;
+  gy = (row_blocks + passes - 1) / passes;
   if (gy > 65535) gy = 65535;
-  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, TY), smem, stream>>>(f);
+  kern<<<dim3(tiles, (unsigned)gy), dim3(32, kLongRows), 0, stream>>>(f);
   return cudaGetLastError();
 }
 
@@ -338,15 +321,15 @@ cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
     case 4 * 4 + 1: return launch_small<4, 1>(f, stream);
     case 4 * 4 + 2: return launch_small<4, 2>(f, stream);
     case 8 * 4 + 1: return launch_small<8, 1>(f, stream);
-    case 8 * 4 + 2: return launch_chunk<8, 2>(f, stream);
-    case 16 * 4 + 1: return launch_chunk<16, 1>(f, stream);
-    case 16 * 4 + 2: return launch_chunk<16, 2>(f, stream);
-    case 32 * 4 + 1: return launch_chunk<32, 1>(f, stream);
-    case 32 * 4 + 2: return launch_chunk<32, 2>(f, stream);
-    case 64 * 4 + 1: return launch_chunk<64, 1>(f, stream);
-    case 64 * 4 + 2: return launch_chunk<64, 2>(f, stream);
-    case 128 * 4 + 1: return launch_chunk<128, 1>(f, stream);
-    case 128 * 4 + 2: return launch_chunk<128, 2>(f, stream);
+    case 8 * 4 + 2: return launch_long<8, 2>(f, stream);
+    case 16 * 4 + 1: return launch_long<16, 1>(f, stream);
+    case 16 * 4 + 2: return launch_long<16, 2>(f, stream);
+    case 32 * 4 + 1: return launch_long<32, 1>(f, stream);
+    case 32 * 4 + 2: return launch_long<32, 2>(f, stream);
+    case 64 * 4 + 1: return launch_long<64, 1>(f, stream);
+    case 64 * 4 + 2: return launch_long<64, 2>(f, stream);
+    case 128 * 4 + 1: return launch_long<128, 1>(f, stream);
+    case 128 * 4 + 2: return launch_long<128, 2>(f, stream);
     default: return cudaErrorInvalidValue;
   }
 }
