@@ -254,26 +254,52 @@ bwd_small_kernel(const BwdParams bp) {
 
 // Long window (W >= 16): blockDim = (32, NCH) with NCH = W / KPT (KPT = 8
 // slots per warp, 16 for W = 256). Warp y owns window slots
-// [KPT y, KPT y + KPT) and lane l owns 2 consecutive columns (4-byte
-// vectors) of a 64-column tile (blockIdx.x), so every load and store of a
-// warp covers 128 contiguous bytes of one token row. The CTA walks rows
+// [KPT y, KPT y + KPT) and lane l owns VC consecutive columns of a
+// (32 VC)-column tile (blockIdx.x), so every load and store of a warp covers
+// 32 VC * 2 contiguous bytes of one token row. The CTA walks rows
 // b = blockIdx.y, blockIdx.y + gridDim.y, ... and per row:
-//   phase 1  z = score + ape, the chunk's max and sum exp per column
+//   phase 1  z = score + ape, the chunk's max m_c and e = exp(z - m_c), sum e
 //   merge    (max, sum) of the NCH chunks of a column, in a fixed order:
-//            NCH/2 threads take 2 chunks each, then a butterfly over those
+//            NCH/VC threads take VC chunks each, then a butterfly over those
 //            lanes (commutative combines, so every lane gets the same bits)
-//   phase 2  p = exp(z - M) / den (one reciprocal per column), the chunk's
-//            share of S = sum (g kv) p
+//   phase 2  p = e * exp(m_c - M) / den (one exp and one reciprocal per column
+//            and chunk), the chunk's share of S = sum (g kv) p
 //   merge    S the same way
 //   phase 3  dscore = p (g kv - S), dkv = g p, stores; dape accumulates in
-//            registers (each thread owns its KPT slots x 2 columns)
-constexpr int kLongVc = 2;   // columns per lane
-
+//            registers (each thread owns its KPT slots x VC columns)
 template <int W>
 struct LongShape {
-  static constexpr int kKpt = W >= 256 ? 16 : 8;  // slots per warp
-  static constexpr int kNch = W / kKpt;           // warps per CTA
+  static constexpr int kKpt = W >= 256 ? 16 : 8;             // slots per warp
+  static constexpr int kVc = (W >= 256 || W <= 16) ? 2 : 4;  // columns per lane
+  static constexpr int kNch = W / kKpt;                      // warps per CTA
   static constexpr int kThreads = 32 * kNch;
+  static constexpr int kMinBlocks = kThreads >= 512 ? 1 : 512 / kThreads;  // <= 128 registers
+  static_assert(kNch % kVc == 0, "each column's chunks split evenly over its merge threads");
+};
+
+template <int VC>
+struct ColVec;
+template <>
+struct ColVec<2> {
+  using T = uint32_t;
+  static __device__ __forceinline__ T load(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint32_t*>(p)); }
+  static __device__ __forceinline__ void store(uint16_t* p, T v) { __stcs(reinterpret_cast<uint32_t*>(p), v); }
+  static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(v, c); }
+  static __device__ __forceinline__ T zero() { return 0u; }
+  static __device__ __forceinline__ T ninf() { return kNegInfBf16x2; }
+  static __device__ __forceinline__ T pack(const float* x) { return pack_bf16x2(x[0], x[1]); }
+};
+template <>
+struct ColVec<4> {
+  using T = uint2;
+  static __device__ __forceinline__ T load(const uint16_t* p) { return ld_stream8(p); }
+  static __device__ __forceinline__ void store(uint16_t* p, T v) { st_stream8(p, v); }
+  static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(c < 2 ? v.x : v.y, c & 1); }
+  static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
+  static __device__ __forceinline__ T ninf() { return make_uint2(kNegInfBf16x2, kNegInfBf16x2); }
+  static __device__ __forceinline__ T pack(const float* x) {
+    return make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  }
 };
 
 // fixed-order merge of (max, sum exp) pairs: m = max, s = s_a e^(m_a - m) + s_b e^(m_b - m)
@@ -287,38 +313,41 @@ __device__ __forceinline__ void merge_max_sum(float& m, float& s, float mb, floa
 }
 
 template <int R, int COFF>
-__global__ void __launch_bounds__(LongShape<COFF * R>::kThreads,
-                                  LongShape<COFF * R>::kThreads >= 512 ? 1 : 2)
+__global__ void __launch_bounds__(LongShape<COFF * R>::kThreads, LongShape<COFF * R>::kMinBlocks)
 bwd_long_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
-  constexpr int kLongKpt = LongShape<W>::kKpt;
+  constexpr int KPT = LongShape<W>::kKpt;
+  constexpr int VC = LongShape<W>::kVc;
   constexpr int NCH = LongShape<W>::kNch;
   constexpr int NT = LongShape<W>::kThreads;
-  constexpr int TC = 32 * kLongVc;      // tile columns
-  constexpr int G = NCH / kLongVc;      // merge threads per column
-  constexpr int LDS = TC + 1;           // padded row stride of the chunk tables
+  constexpr int TC = 32 * VC;      // tile columns
+  constexpr int G = NCH / VC;      // merge threads per column
+  constexpr int LDS = TC + 1;      // padded row stride of the chunk tables
   using S = Slot<R, COFF>;
+  using V = ColVec<VC>;
   const Problem& p = bp.p;
   const int d = p.d;
   const int lane = threadIdx.x, y = threadIdx.y;
   const int tid = y * 32 + lane;
-  const int ncv = d / kLongVc;
+  const int ncv = d / VC;
   const int cv = blockIdx.x * 32 + lane;
   const bool col_ok = cv < ncv;
   const int64_t ld = (int64_t)COFF * d;
-  const int j0 = cv * kLongVc;
-  const int k0 = y * kLongKpt;
+  const int j0 = cv * VC;
+  const int k0 = y * KPT;
   const float kNegInf = __int_as_float(0xff800000);
 
   __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
   __shared__ float M_s[TC], D_s[TC], S_s[TC];
 
-  // this thread's APE values (slots k0.., columns j0, j0+1) are re-read per row through L1
+  // this thread's APE values (slots k0.., columns j0..) are re-read per row through L1
   const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
 
-  float dacc[kLongKpt][kLongVc];
+  float dacc[KPT][VC];
 #pragma unroll
-  for (int t = 0; t < kLongKpt; ++t) dacc[t][0] = dacc[t][1] = 0.0f;
+  for (int t = 0; t < KPT; ++t)
+#pragma unroll
+    for (int c = 0; c < VC; ++c) dacc[t][c] = 0.0f;
 
   // merge thread layout: column mc of the tile, group member mq (G per column)
   const int mc = tid / G, mq = tid % G;
@@ -332,41 +361,52 @@ bwd_long_kernel(const BwdParams bp) {
     const int64_t off = ri.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
     if (b < p.C) {
       // phase 1
-      uint32_t kvw[kLongKpt], scw[kLongKpt];
+      typename V::T kvw[KPT], scw[KPT];
 #pragma unroll
-      for (int t = 0; t < kLongKpt; ++t) {
-        kvw[t] = active ? __ldcs(reinterpret_cast<const uint32_t*>(p.kv + off + t * ld)) : 0u;
-        scw[t] = active ? __ldcs(reinterpret_cast<const uint32_t*>(p.score + off + t * ld))
-                        : kNegInfBf16x2;
+      for (int t = 0; t < KPT; ++t) {
+        kvw[t] = active ? V::load(p.kv + off + t * ld) : V::zero();
+        scw[t] = active ? V::load(p.score + off + t * ld) : V::ninf();
       }
-      const uint32_t gw = col_ok ? __ldcs(reinterpret_cast<const uint32_t*>(bp.grad_out + b * d + j0)) : 0u;
-      float pz[kLongKpt][kLongVc];
+      float g[VC];
+      {
+        const typename V::T gw = col_ok ? V::load(bp.grad_out + b * d + j0) : V::zero();
 #pragma unroll
-      for (int t = 0; t < kLongKpt; ++t) {
-        const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld))
-                                : make_float2(0.0f, 0.0f);
-        pz[t][0] = __fadd_rn(bf16_lo(scw[t]), a.x);
-        pz[t][1] = __fadd_rn(bf16_hi(scw[t]), a.y);
+        for (int c = 0; c < VC; ++c) g[c] = V::elem(gw, c);
       }
+      float pz[KPT][VC];
 #pragma unroll
-      for (int c = 0; c < kLongVc; ++c) {
+      for (int t = 0; t < KPT; ++t) {
+#pragma unroll
+        for (int c = 0; c < VC; c += 2) {
+          const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld + c))
+                                  : make_float2(0.0f, 0.0f);
+          pz[t][c] = __fadd_rn(V::elem(scw[t], c), a.x);
+          pz[t][c + 1] = __fadd_rn(V::elem(scw[t], c + 1), a.y);
+        }
+      }
+      float mloc[VC];
+#pragma unroll
+      for (int c = 0; c < VC; ++c) {
         float m = pz[0][c];
 #pragma unroll
-        for (int t = 1; t < kLongKpt; ++t) m = max_nan(m, pz[t][c]);
+        for (int t = 1; t < KPT; ++t) m = max_nan(m, pz[t][c]);
+        const float mu = m == kNegInf ? 0.0f : m;  // an all -inf chunk contributes 0
         float sum = 0.0f;
-        if (m != kNegInf) {  // an all -inf chunk contributes nothing
 #pragma unroll
-          for (int t = 0; t < kLongKpt; ++t) sum = __fadd_rn(sum, softmax_exp(__fsub_rn(pz[t][c], m)));
+        for (int t = 0; t < KPT; ++t) {
+          pz[t][c] = softmax_exp(__fsub_rn(pz[t][c], mu));
+          sum = __fadd_rn(sum, pz[t][c]);
         }
-        m_s[y * LDS + lane * kLongVc + c] = m;
-        d_s[y * LDS + lane * kLongVc + c] = sum;
+        mloc[c] = m;
+        m_s[y * LDS + lane * VC + c] = m;
+        d_s[y * LDS + lane * VC + c] = sum;
       }
       __syncthreads();
       {
-        float m = m_s[(mq * kLongVc) * LDS + mc], sm = d_s[(mq * kLongVc) * LDS + mc];
+        float m = m_s[(mq * VC) * LDS + mc], sm = d_s[(mq * VC) * LDS + mc];
 #pragma unroll
-        for (int i = 1; i < kLongVc; ++i)
-          merge_max_sum(m, sm, m_s[(mq * kLongVc + i) * LDS + mc], d_s[(mq * kLongVc + i) * LDS + mc]);
+        for (int i = 1; i < VC; ++i)
+          merge_max_sum(m, sm, m_s[(mq * VC + i) * LDS + mc], d_s[(mq * VC + i) * LDS + mc]);
 #pragma unroll
         for (int mask = 1; mask < G; mask <<= 1)
           merge_max_sum(m, sm, __shfl_xor_sync(0xffffffffu, m, mask),
@@ -378,56 +418,57 @@ bwd_long_kernel(const BwdParams bp) {
       }
       __syncthreads();
       // phase 2
-      float g[kLongVc], ssum[kLongVc];
-      g[0] = bf16_lo(gw);
-      g[1] = bf16_hi(gw);
 #pragma unroll
-      for (int c = 0; c < kLongVc; ++c) {
-        const float M = M_s[lane * kLongVc + c];
-        const float den = D_s[lane * kLongVc + c];
+      for (int c = 0; c < VC; ++c) {
+        const float M = M_s[lane * VC + c];
+        const float den = D_s[lane * VC + c];
         const float mu = M == kNegInf ? 0.0f : M;
+        const float ml = mloc[c] == kNegInf ? 0.0f : mloc[c];
+        const float f = softmax_exp(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
         const float yr = __frcp_rn(den);
         float acc = 0.0f;
 #pragma unroll
-        for (int t = 0; t < kLongKpt; ++t) {
-          pz[t][c] = div_rn_by_rcp(softmax_exp(__fsub_rn(pz[t][c], mu)), den, yr);
-          const float dp = __fmul_rn(g[c], bf16_at(kvw[t], c));
+        for (int t = 0; t < KPT; ++t) {
+          pz[t][c] = div_rn_by_rcp(__fmul_rn(pz[t][c], f), den, yr);
+          const float dp = __fmul_rn(g[c], V::elem(kvw[t], c));
           acc = __fadd_rn(acc, __fmul_rn(dp, pz[t][c]));
         }
-        ssum[c] = acc;
-        s_s[y * LDS + lane * kLongVc + c] = acc;
+        s_s[y * LDS + lane * VC + c] = acc;
       }
-      (void)ssum;
       __syncthreads();
       {
-        float sm = s_s[(mq * kLongVc) * LDS + mc];
+        float sm = s_s[(mq * VC) * LDS + mc];
 #pragma unroll
-        for (int i = 1; i < kLongVc; ++i) sm = __fadd_rn(sm, s_s[(mq * kLongVc + i) * LDS + mc]);
+        for (int i = 1; i < VC; ++i) sm = __fadd_rn(sm, s_s[(mq * VC + i) * LDS + mc]);
 #pragma unroll
         for (int mask = 1; mask < G; mask <<= 1) sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, mask));
         if (mq == 0) S_s[mc] = sm;
       }
       __syncthreads();
       // phase 3
-      const float S0 = S_s[lane * kLongVc], S1 = S_s[lane * kLongVc + 1];
+      float Sv[VC];
 #pragma unroll
-      for (int t = 0; t < kLongKpt; ++t) {
-        const float dz0 = __fmul_rn(pz[t][0], __fsub_rn(__fmul_rn(g[0], bf16_lo(kvw[t])), S0));
-        const float dz1 = __fmul_rn(pz[t][1], __fsub_rn(__fmul_rn(g[1], bf16_hi(kvw[t])), S1));
-        dacc[t][0] = __fadd_rn(dacc[t][0], dz0);
-        dacc[t][1] = __fadd_rn(dacc[t][1], dz1);
+      for (int c = 0; c < VC; ++c) Sv[c] = S_s[lane * VC + c];
+#pragma unroll
+      for (int t = 0; t < KPT; ++t) {
+        float dz[VC], dk[VC];
+#pragma unroll
+        for (int c = 0; c < VC; ++c) {
+          dz[c] = __fmul_rn(pz[t][c], __fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]));
+          dk[c] = __fmul_rn(g[c], pz[t][c]);
+          dacc[t][c] = __fadd_rn(dacc[t][c], dz[c]);
+        }
         if (active) {
-          __stcs(reinterpret_cast<uint32_t*>(bp.dkv + off + t * ld),
-                 pack_bf16x2(__fmul_rn(g[0], pz[t][0]), __fmul_rn(g[1], pz[t][1])));
-          __stcs(reinterpret_cast<uint32_t*>(bp.dscore + off + t * ld), pack_bf16x2(dz0, dz1));
+          V::store(bp.dkv + off + t * ld, V::pack(dk));
+          V::store(bp.dscore + off + t * ld, V::pack(dz));
         }
       }
     } else if (active) {
       // a row past capacity has no output slot: zero gradient at its positions
 #pragma unroll
-      for (int t = 0; t < kLongKpt; ++t) {
-        __stcs(reinterpret_cast<uint32_t*>(bp.dkv + off + t * ld), 0u);
-        __stcs(reinterpret_cast<uint32_t*>(bp.dscore + off + t * ld), 0u);
+      for (int t = 0; t < KPT; ++t) {
+        V::store(bp.dkv + off + t * ld, V::zero());
+        V::store(bp.dscore + off + t * ld, V::zero());
       }
     }
     if (ri.last) {
@@ -451,9 +492,8 @@ bwd_long_kernel(const BwdParams bp) {
         }
         const int col_v = blockIdx.x * 32 + x;
         if (col_v >= ncv) continue;
-        const int64_t o = tok * ld + h * d + col_v * kLongVc;
-        __stcs(reinterpret_cast<uint32_t*>(bp.dkv + o), 0u);
-        __stcs(reinterpret_cast<uint32_t*>(bp.dscore + o), 0u);
+        V::store(bp.dkv + tok * ld + h * d + col_v * VC, V::zero());
+        V::store(bp.dscore + tok * ld + h * d + col_v * VC, V::zero());
       }
     }
   }
@@ -462,11 +502,13 @@ bwd_long_kernel(const BwdParams bp) {
 
   // each (slot, column) of the tile belongs to exactly one thread
   if (col_ok) {
-    float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
+    float* part = bp.partial + (int64_t)blockIdx.y * (R * ld) + (int64_t)S::ape_row(k0) * ld +
+                  S::half(k0) * d + j0;
 #pragma unroll
-    for (int t = 0; t < kLongKpt; ++t)
-      *reinterpret_cast<float2*>(part + (int64_t)S::ape_row(k0 + t) * ld + S::half(k0) * d + j0) =
-          make_float2(dacc[t][0], dacc[t][1]);
+    for (int t = 0; t < KPT; ++t)
+#pragma unroll
+      for (int c = 0; c < VC; c += 2)
+        *reinterpret_cast<float2*>(part + t * ld + c) = make_float2(dacc[t][c], dacc[t][c + 1]);
   }
 }
 
@@ -539,7 +581,7 @@ template <int R, int COFF>
 cudaError_t plan_long(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
   constexpr int NT = LongShape<W>::kThreads;
-  const int ncv = p.d / kLongVc;
+  const int ncv = p.d / LongShape<W>::kVc;
   const int tiles = (ncv + 31) / 32;
   auto kern = bwd_long_kernel<R, COFF>;
   const int occ = occupancy(kern, NT, 0);
