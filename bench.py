@@ -289,6 +289,111 @@ def run_reference(args, rank, world):
     return 0
 
 
+class Ranks:
+    """Ranks of a torchrun job (one process per GPU, replicas of the workload):
+    a barrier and the max of a value over ranks through a process group when
+    WORLD_SIZE > 1, no-ops for a single process."""
+
+    def __init__(self, rank: int, world: int, backend: str = "nccl", device=None):
+        self.rank, self.world, self.backend, self.device = rank, world, backend, device
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            if not dist.is_initialized():
+                kw = {"device_id": device} if backend == "nccl" and device is not None else {}
+                dist.init_process_group(backend, **kw)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        where = self.device if self.backend == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=where)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def run_e2e(args, case, dev, stream, ranks):
+    """Pipelined end-to-end loop through the C ABI (see the call site)."""
+    import numpy as np
+    import torch
+
+    import gated_softmax_kv_gb300 as gsk
+
+    T, C, r, coff, d = case.total_tokens, case.capacity, case.ratio, case.coff, case.head_dim
+
+    def pinned(a, dtype):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype == torch.bfloat16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.pin_memory()
+
+    h_in = [pinned(case.kv, torch.bfloat16), pinned(case.score, torch.bfloat16),
+            pinned(case.grad_out, torch.bfloat16), pinned(case.ape, torch.float32),
+            pinned(case.cu_seqlens, torch.int32), pinned(case.cu_seqlens_comp, torch.int32)]
+    d_in = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in h_in] for _ in range(2)]
+    out_shapes = [((C, d), torch.bfloat16), ((T, coff * d), torch.bfloat16),
+                  ((T, coff * d), torch.bfloat16), ((r, coff * d), torch.float32)]
+    d_out = [[torch.empty(sh, dtype=dt, device=dev) for sh, dt in out_shapes] for _ in range(2)]
+    h_out = [[torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in out_shapes] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    sh = int(stream.cuda_stream)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+    used = [False, False]
+
+    def step(i):
+        s = i % 2
+        kv, score, go, ape, cu, cuc = d_in[s]
+        out, dkv, dscore, dape = d_out[s]
+        with torch.cuda.stream(s_h2d):
+            if used[s]:
+                s_h2d.wait_event(ev["comp"][s])   # step i-2 finished reading this set
+            for dt, ht in zip(d_in[s], h_in):
+                dt.copy_(ht, non_blocking=True)
+            ev["in"][s].record(s_h2d)
+        stream.wait_event(ev["in"][s])
+        if used[s]:
+            stream.wait_event(ev["out"][s])       # step i-2's results have left this set
+        gsk.csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
+                                 cuc.data_ptr(), case.num_seqs, T, C, r, coff, d, out.data_ptr(), sh)
+        gsk.csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
+                                 cuc.data_ptr(), case.num_seqs, T, C, r, coff, d, go.data_ptr(),
+                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh)
+        ev["comp"][s].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev["comp"][s])
+            for dt, ht in zip(d_out[s], h_out[s]):
+                ht.copy_(dt, non_blocking=True)
+            ev["out"][s].record(s_d2h)
+        used[s] = True
+
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
+    KE = max(1, args.e2e_steps)
+    ranks.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(KE):
+        step(i)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    el = ranks.max(el)
+    return el, h2d, d2h, KE
+
+
 def run_gpu(args, rank, world, local):
     import numpy as np
     import torch
@@ -298,11 +403,7 @@ def run_gpu(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
+    ranks = Ranks(rank, world, "nccl", dev)
 
     gsk.build()
     lib = gsk.load()  # noqa: F841  (fails loudly if the library is missing)
@@ -333,9 +434,7 @@ def run_gpu(args, rank, world, local):
                                  cuc.data_ptr(), nseq, T, C, r, coff, d, grad_out.data_ptr(),
                                  dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh)
 
-    def barrier():
-        if pg is not None:
-            pg.barrier()
+    barrier = ranks.barrier
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -363,58 +462,17 @@ def run_gpu(args, rank, world, local):
     elapsed = start.elapsed_time(end) / 1e3
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    if pg is not None:
-        t = torch.tensor([elapsed], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = ranks.max(elapsed)
 
-    # end to end through the same C ABI with host buffers: pinned host -> HBM
-    # copies of every input, both calls, and every result back to the host
-    h_kv = torch.empty(kv.shape, dtype=torch.bfloat16, pin_memory=True).copy_(kv)
-    h_score = torch.empty(score.shape, dtype=torch.bfloat16, pin_memory=True).copy_(score)
-    h_go = torch.empty(grad_out.shape, dtype=torch.bfloat16, pin_memory=True).copy_(grad_out)
-    h_ape = torch.empty(ape.shape, dtype=torch.float32, pin_memory=True).copy_(ape)
-    h_cu = torch.empty(cu.shape, dtype=torch.int32, pin_memory=True).copy_(cu)
-    h_cuc = torch.empty(cuc.shape, dtype=torch.int32, pin_memory=True).copy_(cuc)
-    h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
-    h_dkv = torch.empty(dkv.shape, dtype=torch.bfloat16, pin_memory=True)
-    h_ds = torch.empty(dscore.shape, dtype=torch.bfloat16, pin_memory=True)
-    h_dape = torch.empty(dape.shape, dtype=torch.float32, pin_memory=True)
-    ins = [(kv, h_kv), (score, h_score), (grad_out, h_go), (ape, h_ape), (cu, h_cu), (cuc, h_cuc)]
-    outs = [(out, h_out), (dkv, h_dkv), (dscore, h_ds), (dape, h_dape)]
-    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
-    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
-
-    def e2e_step():
-        for dt, ht in ins:
-            dt.copy_(ht, non_blocking=True)
-        fwd()
-        bwd()
-        for dt, ht in outs:
-            ht.copy_(dt, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    KE = max(1, args.e2e_steps)
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(KE):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if pg is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    barrier()
+    # End to end through the same C ABI with host buffers. Every step copies its
+    # inputs from pinned host memory to HBM, runs both calls and copies every
+    # result back. Consecutive steps overlap: two device buffer sets, H2D and D2H
+    # on their own streams, ordered against the compute stream by events (the
+    # H2D of step i+1 and the D2H of step i-1 run while step i computes).
+    e2e_s, h2d, d2h, KE = run_e2e(args, case, dev, stream, ranks)
 
     if rank != 0:
-        if pg is not None:
-            pg.destroy_process_group()
+        ranks.close()
         return 0
 
     fwd_bytes, bwd_bytes = algorithmic_bytes(case)
@@ -457,8 +515,7 @@ def run_gpu(args, rank, world, local):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    ranks.close()
     return 0
 
 

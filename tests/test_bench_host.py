@@ -1,0 +1,76 @@
+"""Host logic of bench.py without a GPU: the multi-rank bookkeeping (barrier
+and max over ranks, as torchrun runs it with one process per GPU) on two
+gloo ranks, the algorithmic byte counts and the reference arm's rank rule."""
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    sys.argv = ["bench.py"]
+    import bench
+    r = bench.Ranks(rank, world, backend="gloo")
+    r.barrier()
+    worst = r.max(1.5 * (rank + 1))   # each rank's elapsed time; the job's is the max
+    r.barrier()
+    r.close()
+    q.put((rank, worst))
+
+
+def test_two_gloo_ranks_take_the_max_elapsed_time():
+    mp = pytest.importorskip("torch.multiprocessing")
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs)
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert got == [(0, 3.0), (1, 3.0)]
+
+
+def test_single_process_ranks_are_noops():
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.Ranks(0, 1)
+    r.barrier()
+    assert r.max(2.5) == 2.5
+
+
+def test_algorithmic_bytes_per_token_at_the_headline():
+    import bench
+    import workloads
+    case = workloads.config("headline", fill=False)
+    fwd, bwd = bench.algorithmic_bytes(case)
+    # kv and score read once (4 B per token column), out written per capacity row
+    assert fwd == 262144 * 1024 * 4 + case.capacity * 512 * 2 + 4 * 1024 * 4
+    # plus dkv / dscore written in full, grad_out of the true rows, dape written
+    assert bwd == 2 * 262144 * 1024 * 4 + case.true_rows * 512 * 2 + 2 * 4 * 1024 * 4
+    assert abs(fwd / 262144 - 4352) / 4352 < 0.01
+    assert abs(bwd / 262144 - 8448) / 8448 < 0.01
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    import bench
+
+    class A:
+        steps, warmup, tokens, workload = 1, 0, 262144, "headline"
+
+    assert bench.run_reference(A(), rank=1, world=2) == 0
+    assert capsys.readouterr().out == ""
