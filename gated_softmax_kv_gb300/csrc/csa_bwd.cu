@@ -32,12 +32,6 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-
-// Resident CTAs per SM the small-window backward is compiled for (sets its
-// register budget: 3 -> 80 registers per thread).
-#ifndef CSA_BWD_SMALL_MIN_BLOCKS
-#define CSA_BWD_SMALL_MIN_BLOCKS 3
-#endif
 constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
 
 
@@ -73,11 +67,10 @@ __device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
 
 // Small window (W <= 8): blockDim = (TX, TY); a thread owns 4 consecutive
 // columns (8-byte vectors) of one row at a time, rows strided by the grid.
-// Its dape sums live in its own shared-memory slots (W float4), which keeps
-// the kernel at three CTAs per SM. D > 0 fixes head_dim at compile time
-// (slot offsets become immediates); D == 0 reads it from the problem.
+// D > 0 fixes head_dim at compile time (slot offsets become immediates);
+// D == 0 reads it from the problem.
 template <int R, int COFF, int D>
-__global__ void __launch_bounds__(kThreads, CSA_BWD_SMALL_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_small_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
@@ -95,18 +88,21 @@ bwd_small_kernel(const BwdParams bp) {
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
-  // [W][tile_cols] APE slice of this column tile, then [W][nthr] float4 dape sums
+  // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
     sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
-  const float* ape_s = sm + tx * kCv;
-  float4* dacc = reinterpret_cast<float4*>(sm + W * tile_cols) + tid;  // slot k at dacc[k * nthr]
-#pragma unroll
-  for (int k = 0; k < W; ++k) dacc[k * nthr] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   __syncthreads();
+  const float* ape_s = sm + tx * kCv;
+
+  float dacc[W][kCv];
+#pragma unroll
+  for (int k = 0; k < W; ++k)
+#pragma unroll
+    for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
 
   const uint2 zero2 = make_uint2(0u, 0u);
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
@@ -179,19 +175,12 @@ bwd_small_kernel(const BwdParams bp) {
           float dz[2], dk[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
             const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
-            dz[h] = __fmul_rn(pz[k][2 * c2 + h], __fsub_rn(dp, sum[h]));
-            dk[h] = __fmul_rn(g[h], pz[k][2 * c2 + h]);
+            dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
+            dk[h] = __fmul_rn(g[h], pz[k][c]);
+            dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);
           }
-          float4 a = dacc[k * nthr];
-          if (c2 == 0) {
-            a.x = __fadd_rn(a.x, dz[0]);
-            a.y = __fadd_rn(a.y, dz[1]);
-          } else {
-            a.z = __fadd_rn(a.z, dz[0]);
-            a.w = __fadd_rn(a.w, dz[1]);
-          }
-          dacc[k * nthr] = a;
           if (c2 == 0) {
             scv[k].x = pack_bf16x2(dz[0], dz[1]);
             kvv[k].x = pack_bf16x2(dk[0], dk[1]);
@@ -240,19 +229,26 @@ bwd_small_kernel(const BwdParams bp) {
 
   zero_orphans(bp, R);
 
-  // combine the TY thread rows in ascending order and write this CTA's slice
-  // of the partial of row group blockIdx.y
+  // combine the TY thread rows in ascending order, then write this CTA's
+  // slice of the partial of row group blockIdx.y
   __syncthreads();
-  const float* dsum = sm + W * tile_cols;  // [W][nthr][4]
+  for (int t = 0; t < TY; ++t) {
+    if (ty == t && col_ok) {
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+#pragma unroll
+        for (int c = 0; c < kCv; ++c) {
+          float* s = sm + k * tile_cols + tx * kCv + c;
+          *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
+        }
+    }
+    __syncthreads();
+  }
   float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
-    const int cc = i - k * tile_cols;
-    const int col = blockIdx.x * tile_cols + cc;
-    if (col >= d) continue;
-    float v = dsum[((int64_t)k * nthr + cc / kCv) * kCv + (cc % kCv)];
-    for (int t = 1; t < TY; ++t) v = __fadd_rn(v, dsum[((int64_t)k * nthr + t * TX + cc / kCv) * kCv + (cc % kCv)]);
-    part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = v;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    if (col < d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = sm[i];
   }
 }
 
@@ -554,7 +550,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const int tx = ncv <= 128 ? ncv : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kCv + sizeof(float) * 4 * W * tx * ty;
+  const size_t smem = sizeof(float) * W * tx * kCv;
   auto kern = bwd_small_kernel<R, COFF, D>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);

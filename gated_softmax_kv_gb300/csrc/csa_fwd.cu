@@ -11,8 +11,8 @@
 // kernel shapes:
 //
 //  * fwd_small (window W = coff*ratio <= 8): a thread owns one output row and
-//    4 consecutive columns. It issues all 2W 8-byte loads of its window up
-//    front (one coalesced 256-byte request per warp per slot), reads its APE
+//    8 consecutive columns. It issues all 2W 16-byte loads of its window up
+//    front (one coalesced 512-byte request per warp per slot), reads its APE
 //    columns from a shared-memory slice staged once per CTA (persistent grid,
 //    rows strided by the whole grid) and evaluates m = max z, e = exp(z - m),
 //    den = sum e in slot order and out = (sum e * kv) / den: one division per
@@ -37,30 +37,23 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Resident CTAs per SM the small-window forward is compiled for (sets its
-// register budget: 3 -> 80 registers per thread).
-#ifndef CSA_FWD_SMALL_MIN_BLOCKS
-#define CSA_FWD_SMALL_MIN_BLOCKS 3
-#endif
-
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
-// D == 0 reads it from the problem. A thread owns 4 columns (8-byte vectors).
+// D == 0 reads it from the problem.
 template <int R, int COFF, int D>
-__global__ void __launch_bounds__(kThreads, CSA_FWD_SMALL_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, 2)
 fwd_small_kernel(const FwdParams f) {
   constexpr int W = COFF * R;
-  constexpr int VC = 4;
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
   const int d = D > 0 ? D : p.d;
   const int TX = blockDim.x, TY = blockDim.y;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int tid = ty * TX + tx, nthr = TX * TY;
-  const int ncv = d / VC;
-  const int cv = blockIdx.x * TX + tx;
+  const int nvec = d / kVec;
+  const int jv = blockIdx.x * TX + tx;
   const int64_t ld = (int64_t)COFF * d;
-  const int j0 = cv * VC;
-  const int tile_cols = TX * VC;
+  const int j0 = jv * kVec;
+  const int tile_cols = TX * kVec;
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
@@ -72,8 +65,8 @@ fwd_small_kernel(const FwdParams f) {
     sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
   __syncthreads();
-  if (cv >= ncv) return;  // no barrier below
-  const float* ape_s = sm + tx * VC;
+  if (jv >= nvec) return;  // no barrier below
+  const float* ape_s = sm + tx * kVec;
 
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
   const int64_t stride = (int64_t)gridDim.y * TY;
@@ -82,50 +75,61 @@ fwd_small_kernel(const FwdParams f) {
     const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     uint16_t* dst = f.out + b * d + j0;
     if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
-      st_stream8(dst, make_uint2(0x7FC07FC0u, 0x7FC07FC0u));
+      st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
       continue;
     }
     const int64_t rowoff = ri.base * ld + j0;
     const uint16_t* kv_row = p.kv + rowoff;
     const uint16_t* sc_row = p.score + rowoff;
-    uint2 kvv[W], scv[W];
+    uint4 kvv[W], scv[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) {
       if (S::masked(ri.first, k)) {  // kv = 0, score = -inf
-        kvv[k] = make_uint2(0u, 0u);
-        scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+        kvv[k] = make_uint4(0u, 0u, 0u, 0u);
+        scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
       } else {
-        kvv[k] = ld_stream8(kv_row + koff(k));
-        scv[k] = ld_stream8(sc_row + koff(k));
+        kvv[k] = ld_stream(kv_row + koff(k));
+        scv[k] = ld_stream(sc_row + koff(k));
       }
     }
     // logits z = score + ape
-    float z[W][VC];
+    float z[W][kVec];
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
-      z[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
-      z[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
-      z[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
-      z[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
+      const float4 a0 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
+      const float4 a1 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols + 4);
+      z[k][0] = __fadd_rn(bf16_lo(scv[k].x), a0.x);
+      z[k][1] = __fadd_rn(bf16_hi(scv[k].x), a0.y);
+      z[k][2] = __fadd_rn(bf16_lo(scv[k].y), a0.z);
+      z[k][3] = __fadd_rn(bf16_hi(scv[k].y), a0.w);
+      z[k][4] = __fadd_rn(bf16_lo(scv[k].z), a1.x);
+      z[k][5] = __fadd_rn(bf16_hi(scv[k].z), a1.y);
+      z[k][6] = __fadd_rn(bf16_lo(scv[k].w), a1.z);
+      z[k][7] = __fadd_rn(bf16_hi(scv[k].w), a1.w);
     }
     // m = max z, e = exp(z - m), den = sum e, out = (sum e * kv) / den
-    float res[VC];
+    uint32_t ow[4];
 #pragma unroll
-    for (int c = 0; c < VC; ++c) {
-      float m = z[0][c];
+    for (int c2 = 0; c2 < 4; ++c2) {
+      float res[2];
 #pragma unroll
-      for (int k = 1; k < W; ++k) m = max_nan(m, z[k][c]);
-      float den = 0.0f, acc = 0.0f;
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * c2 + h;
+        float m = z[0][c];
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const float e = softmax_exp(__fsub_rn(z[k][c], m));
-        den = __fadd_rn(den, e);
-        acc = __fmaf_rn(e, bf16_at(c < 2 ? kvv[k].x : kvv[k].y, c & 1), acc);
+        for (int k = 1; k < W; ++k) m = max_nan(m, z[k][c]);
+        float den = 0.0f, acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const float e = softmax_exp(__fsub_rn(z[k][c], m));
+          den = __fadd_rn(den, e);
+          acc = __fmaf_rn(e, bf16_elem(kvv[k], c), acc);
+        }
+        res[h] = __fdiv_rn(acc, den);
       }
-      res[c] = __fdiv_rn(acc, den);
+      ow[c2] = pack_bf16x2(res[0], res[1]);
     }
-    st_stream8(dst, make_uint2(pack_bf16x2(res[0], res[1]), pack_bf16x2(res[2], res[3])));
+    st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
   }
 }
 
@@ -252,11 +256,11 @@ int occupancy(K kernel, int threads, size_t smem) {
 template <int R, int COFF, int D>
 cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   constexpr int W = COFF * R;
-  const int ncv = f.p.d / 4;
-  const int tx = ncv <= 128 ? ncv : 128;
+  const int nvec = f.p.d / kVec;
+  const int tx = nvec <= 128 ? nvec : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
-  const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * 4;
+  const int tiles = (nvec + tx - 1) / tx;
+  const size_t smem = sizeof(float) * W * tx * kVec;
   auto kern = fwd_small_kernel<R, COFF, D>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
