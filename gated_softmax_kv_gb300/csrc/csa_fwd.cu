@@ -28,6 +28,7 @@
 
 #include <mutex>
 
+#include "csa_async.cuh"
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -130,6 +131,170 @@ fwd_small_kernel(const FwdParams f) {
       ow[c2] = pack_bf16x2(res[0], res[1]);
     }
     st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+  }
+}
+
+// Producer/consumer forward (W <= 8, 256 <= head_dim <= 2048). One producer
+// warp streams each row's window -- 2W pieces of head_dim bf16 (kv and score
+// rows of the window's tokens, in the window's column half) -- into a ring of
+// shared-memory stages with bulk asynchronous copies (TMA engine), counted on
+// a per-stage "full" mbarrier. Eight consumer warps compute the rows of a
+// stage from shared memory (a thread owns 8 columns of one row, its APE
+// columns in registers) and release the stage on its "empty" mbarrier. The
+// loads of the next stages stay in flight while the current one is computed.
+// Same arithmetic as fwd_small_kernel. Chunk q of rows [q rs, q rs + rs) goes
+// to CTA q mod gridDim.x.
+constexpr int kPcConsumers = 256;               // 8 consumer warps
+constexpr int kPcThreads = kPcConsumers + 32;   // + 1 producer warp
+constexpr size_t kPcRingBytes = 192 * 1024;     // shared-memory budget of the stage ring
+
+#ifndef CSA_FWD_PC
+#define CSA_FWD_PC 1
+#endif
+
+template <int R, int COFF>
+__global__ void __launch_bounds__(kPcThreads, 1)
+fwd_small_pc_kernel(const FwdParams f, int ns) {
+  constexpr int W = COFF * R;
+  using S = Slot<R, COFF>;
+  const Problem& p = f.p;
+  const int d = p.d;
+  const int txc = d / kVec;            // consumer threads per row
+  const int rs = kPcConsumers / txc;   // rows per chunk
+  const int64_t ld = (int64_t)COFF * d;
+  const int64_t row_elems = (int64_t)2 * W * d;  // [kv | score][slot][head_dim]
+  const int64_t stage_elems = row_elems * rs;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint16_t* stages = reinterpret_cast<uint16_t*>(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)ns * stage_elems * 2);
+  uint64_t* empty = full + ns;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t nchunks = (p.C + rs - 1) / rs;
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+
+  if (tid == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kPcConsumers / 32);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kPcConsumers / 32) {
+    // producer: lane r (< rs) fetches row r of each chunk
+    int hint = 0;
+    int64_t n = 0;
+    for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++n) {
+      const int s = (int)(n % ns);
+      const uint32_t use = (uint32_t)(n / ns);
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, f.faults)) break;
+      const int64_t b = q * rs + lane;
+      bool fetch = false;
+      RowInfo ri;
+      uint32_t bytes = 0;
+      if (lane < rs && b < p.C) {
+        ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+        fetch = row_in_bounds<R, COFF>(ri, p.T);
+        if (fetch) {
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            if (!S::masked(ri.first, k)) bytes += 2u * (uint32_t)d * 2u;
+        }
+      }
+      uint32_t total = bytes;
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+      __syncwarp();
+      if (fetch) {
+        uint16_t* dst = stages + s * stage_elems + lane * row_elems;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          if (S::masked(ri.first, k)) continue;
+          const int64_t src = S::tok(ri.base, k) * ld + S::half(k) * d;
+          bulk_g2s(dst + (int64_t)k * d, p.kv + src, (uint32_t)d * 2u, &full[s]);
+          bulk_g2s(dst + (int64_t)(W + k) * d, p.score + src, (uint32_t)d * 2u, &full[s]);
+        }
+      }
+    }
+    // no copy into this CTA's shared memory may be in flight when it exits:
+    // wait for the last fill of every stage (bounded)
+    for (int64_t m = n > ns ? n - ns : 0; m < n; ++m)
+      mbar_wait(&full[m % ns], (uint32_t)(m / ns) & 1u, f.faults);
+    return;
+  }
+
+  // consumers: thread (r, tx) owns columns 8 tx .. 8 tx + 7 of row r of each chunk
+  const int r = tid / txc, tx = tid - (tid / txc) * txc;
+  const bool active = r < rs;
+  const int j0 = tx * kVec;
+  float apev[W][kVec];
+#pragma unroll
+  for (int k = 0; k < W; ++k) {
+    if (active) {
+      const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + j0;
+      const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
+      apev[k][0] = lo.x; apev[k][1] = lo.y; apev[k][2] = lo.z; apev[k][3] = lo.w;
+      apev[k][4] = hi.x; apev[k][5] = hi.y; apev[k][6] = hi.z; apev[k][7] = hi.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < kVec; ++c) apev[k][c] = 0.0f;
+    }
+  }
+  int hint = 0;
+  int64_t n = 0;
+  for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++n) {
+    const int s = (int)(n % ns);
+    if (!mbar_wait(&full[s], (uint32_t)(n / ns) & 1u, f.faults)) break;
+    const int64_t b = q * rs + r;
+    if (active && b < p.C) {
+      const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+      uint16_t* dst = f.out + b * d + j0;
+      if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
+        st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
+      } else {
+        const uint16_t* src = stages + s * stage_elems + r * row_elems + j0;
+        uint4 kvv[W], scv[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          if (S::masked(ri.first, k)) {
+            kvv[k] = make_uint4(0u, 0u, 0u, 0u);
+            scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+          } else {
+            kvv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)k * d);
+            scv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)(W + k) * d);
+          }
+        }
+        uint32_t ow[4];
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) {
+          float res[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;
+            float z[W];
+#pragma unroll
+            for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), apev[k][c]);
+            float m = z[0];
+#pragma unroll
+            for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
+            float den = 0.0f, acc = 0.0f;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              const float e = softmax_exp(__fsub_rn(z[k], m));
+              den = __fadd_rn(den, e);
+              acc = __fmaf_rn(e, bf16_elem(kvv[k], c), acc);
+            }
+            res[h] = __fdiv_rn(acc, den);
+          }
+          ow[c2] = pack_bf16x2(res[0], res[1]);
+        }
+        st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -278,7 +443,33 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
 }
 
 template <int R, int COFF>
+cudaError_t launch_small_pc(const FwdParams& f, cudaStream_t stream, bool* launched) {
+  constexpr int W = COFF * R;
+  *launched = false;
+  const int d = f.p.d;
+  if (!CSA_FWD_PC || d < 256 || d > 2048 || f.p.C == 0) return cudaSuccess;
+  const int rs = kPcConsumers / (d / kVec);
+  const size_t stage_bytes = (size_t)rs * 2 * W * d * 2;
+  int ns = (int)(kPcRingBytes / stage_bytes);
+  if (ns > 8) ns = 8;
+  if (ns < 2) return cudaSuccess;
+  const size_t smem = (size_t)ns * stage_bytes + 2 * (size_t)ns * sizeof(uint64_t);
+  auto kern = fwd_small_pc_kernel<R, COFF>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t nchunks = (f.p.C + rs - 1) / rs;
+  int64_t grid = sm_count();
+  if (grid > nchunks) grid = nchunks;
+  kern<<<(unsigned)grid, kPcThreads, smem, stream>>>(f, ns);
+  *launched = true;
+  return cudaGetLastError();
+}
+
+template <int R, int COFF>
 cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
+  bool launched = false;
+  cudaError_t e = launch_small_pc<R, COFF>(f, stream, &launched);
+  if (e != cudaSuccess || launched) return e;
   if (f.p.d == 512) return launch_small_d<R, COFF, 512>(f, stream);
   if (f.p.d == 128) return launch_small_d<R, COFF, 128>(f, stream);
   return launch_small_d<R, COFF, 0>(f, stream);

@@ -26,6 +26,7 @@ struct Problem {
 struct FwdParams {
   Problem p;
   uint16_t* out;           // [C, d]
+  unsigned int* faults;    // device fault word (bounded waits that gave up)
 };
 
 struct BwdParams {
@@ -56,6 +57,9 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+
+// Device address of the fault word on the current device (csa_async.cu).
+cudaError_t device_fault_word(unsigned int** out);
 
 }  // namespace csa
 
