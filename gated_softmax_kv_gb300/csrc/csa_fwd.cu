@@ -152,6 +152,8 @@ constexpr size_t kPcRingBytes = 192 * 1024;     // shared-memory budget of the s
 #define CSA_FWD_PC 1
 #endif
 
+constexpr int kPcSegCache = 2048;  // segment-array entries staged in shared memory
+
 template <int R, int COFF>
 __global__ void __launch_bounds__(kPcThreads, 1)
 fwd_small_pc_kernel(const FwdParams f, int ns) {
@@ -160,7 +162,7 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
   const Problem& p = f.p;
   const int d = p.d;
   const int txc = d / kVec;            // consumer threads per row
-  const int rs = kPcConsumers / txc;   // rows per chunk
+  const int rs = kPcConsumers / txc;   // rows per chunk (<= 8)
   const int64_t ld = (int64_t)COFF * d;
   const int64_t row_elems = (int64_t)2 * W * d;  // [kv | score][slot][head_dim]
   const int64_t stage_elems = row_elems * rs;
@@ -168,9 +170,21 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
   uint16_t* stages = reinterpret_cast<uint16_t*>(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)ns * stage_elems * 2);
   uint64_t* empty = full + ns;
+  __shared__ int32_t cu_s[kPcSegCache], cuc_s[kPcSegCache];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nchunks = (p.C + rs - 1) / rs;
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  // segment arrays: staged in shared memory when they fit (row lookups then
+  // cost no global round trip), else read from global memory
+  const bool seg_cached = p.nseq + 1 <= kPcSegCache;
+  if (seg_cached) {
+    for (int i = tid; i <= p.nseq; i += kPcThreads) {
+      cu_s[i] = __ldg(p.cu + i);
+      cuc_s[i] = __ldg(p.cuc + i);
+    }
+  }
+  const int32_t* cu = seg_cached ? cu_s : p.cu;
+  const int32_t* cuc = seg_cached ? cuc_s : p.cuc;
 
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -182,7 +196,8 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
   __syncthreads();
 
   if (warp == kPcConsumers / 32) {
-    // producer: lane r (< rs) fetches row r of each chunk
+    // producer: lane r (< rs) looks up row r of each chunk; all 32 lanes share
+    // the 2W copies per row
     int hint = 0;
     int64_t n = 0;
     for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++n) {
@@ -192,9 +207,11 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
       const int64_t b = q * rs + lane;
       bool fetch = false;
       RowInfo ri;
+      ri.base = 0;
+      ri.first = true;
       uint32_t bytes = 0;
       if (lane < rs && b < p.C) {
-        ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+        ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
         fetch = row_in_bounds<R, COFF>(ri, p.T);
         if (fetch) {
 #pragma unroll
@@ -207,14 +224,19 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
       for (int m = 16; m > 0; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
       if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
       __syncwarp();
-      if (fetch) {
-        uint16_t* dst = stages + s * stage_elems + lane * row_elems;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          if (S::masked(ri.first, k)) continue;
-          const int64_t src = S::tok(ri.base, k) * ld + S::half(k) * d;
-          bulk_g2s(dst + (int64_t)k * d, p.kv + src, (uint32_t)d * 2u, &full[s]);
-          bulk_g2s(dst + (int64_t)(W + k) * d, p.score + src, (uint32_t)d * 2u, &full[s]);
+      // lanes [r g, r g + g) copy the 2W pieces of row r (g = 32 / rs lanes per row)
+      const int g = 32 / rs;
+      const int my_row = lane / g < rs ? lane / g : 0;
+      const int64_t base = __shfl_sync(0xffffffffu, ri.base, my_row);
+      const int first = __shfl_sync(0xffffffffu, (int)ri.first, my_row);
+      const int ok = __shfl_sync(0xffffffffu, (int)fetch, my_row);
+      if (lane / g < rs && ok) {
+        for (int j = lane % g; j < 2 * W; j += g) {
+          const int k = j >> 1, t = j & 1;
+          if (S::masked(first != 0, k)) continue;
+          const int64_t src = S::tok(base, k) * ld + S::half(k) * d;
+          uint16_t* dst = stages + s * stage_elems + my_row * row_elems + (int64_t)(t * W + k) * d;
+          bulk_g2s(dst, (t ? p.score : p.kv) + src, (uint32_t)d * 2u, &full[s]);
         }
       }
     }
@@ -249,7 +271,7 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
     if (!mbar_wait(&full[s], (uint32_t)(n / ns) & 1u, f.faults)) break;
     const int64_t b = q * rs + r;
     if (active && b < p.C) {
-      const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+      const RowInfo ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
       uint16_t* dst = f.out + b * d + j0;
       if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
         st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
