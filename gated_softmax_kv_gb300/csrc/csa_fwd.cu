@@ -134,11 +134,12 @@ fwd_small_kernel(const FwdParams f) {
   }
 }
 
-// Producer/consumer forward (W <= 8, 256 <= head_dim <= 2048). One producer
-// warp streams each row's window -- 2W pieces of head_dim bf16 (kv and score
-// rows of the window's tokens, in the window's column half) -- into a ring of
-// shared-memory stages with bulk asynchronous copies (TMA engine), counted on
-// a per-stage "full" mbarrier. Eight consumer warps compute the rows of a
+// Producer/consumer forward (W <= 8, 256 <= head_dim <= 2048, head_dim a
+// multiple of 256). One producer warp streams each row's window into a ring
+// of shared-memory stages with 2D tensor-map copies (TMA engine): per tensor
+// and window half, tiles of [ratio tokens x 256 columns] (2 KB at ratio 4;
+// 1 KB pieces measured well below the 2 KB rate on this GPU), counted on a
+// per-stage "full" mbarrier. Eight consumer warps compute the rows of a
 // stage from shared memory (a thread owns 8 columns of one row, its APE
 // columns in registers) and release the stage on its "empty" mbarrier. The
 // loads of the next stages stay in flight while the current one is computed.
@@ -156,7 +157,8 @@ constexpr int kPcSegCache = 2048;  // segment-array entries staged in shared mem
 
 template <int R, int COFF>
 __global__ void __launch_bounds__(kPcThreads, 1)
-fwd_small_pc_kernel(const FwdParams f, int ns) {
+fwd_small_pc_kernel(const FwdParams f, int ns, const __grid_constant__ CUtensorMap tm_kv,
+                    const __grid_constant__ CUtensorMap tm_sc, int bx) {
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
@@ -164,11 +166,16 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
   const int txc = d / kVec;            // consumer threads per row
   const int rs = kPcConsumers / txc;   // rows per chunk (<= 8)
   const int64_t ld = (int64_t)COFF * d;
-  const int64_t row_elems = (int64_t)2 * W * d;  // [kv | score][slot][head_dim]
+  const int ncb = d / bx;  // column boxes per window half
+  // row layout: [kv | score][window half g][column box][token of the block][bx]
+  const int64_t row_elems = (int64_t)2 * W * d;
   const int64_t stage_elems = row_elems * rs;
+  const uint32_t box_bytes = (uint32_t)R * (uint32_t)bx * 2u;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint16_t* stages = reinterpret_cast<uint16_t*>(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)ns * stage_elems * 2);
+  // tiles land 128-byte aligned (the launch adds 128 bytes of slack)
+  uint8_t* smem_al = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint16_t* stages = reinterpret_cast<uint16_t*>(smem_al);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_al + (size_t)ns * stage_elems * 2);
   uint64_t* empty = full + ns;
   __shared__ int32_t cu_s[kPcSegCache], cuc_s[kPcSegCache];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -213,11 +220,8 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
       if (lane < rs && b < p.C) {
         ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
         fetch = row_in_bounds<R, COFF>(ri, p.T);
-        if (fetch) {
-#pragma unroll
-          for (int k = 0; k < W; ++k)
-            if (!S::masked(ri.first, k)) bytes += 2u * (uint32_t)d * 2u;
-        }
+        if (fetch)  // both tensors, every column box, of each loaded window half
+          bytes = (uint32_t)(COFF == 2 && ri.first ? 1 : COFF) * (uint32_t)ncb * 2u * box_bytes;
       }
       uint32_t total = bytes;
 #pragma unroll
@@ -231,12 +235,15 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
       const int first = __shfl_sync(0xffffffffu, (int)ri.first, my_row);
       const int ok = __shfl_sync(0xffffffffu, (int)fetch, my_row);
       if (lane / g < rs && ok) {
-        for (int j = lane % g; j < 2 * W; j += g) {
-          const int k = j >> 1, t = j & 1;
-          if (S::masked(first != 0, k)) continue;
-          const int64_t src = S::tok(base, k) * ld + S::half(k) * d;
-          uint16_t* dst = stages + s * stage_elems + my_row * row_elems + (int64_t)(t * W + k) * d;
-          bulk_g2s(dst, (t ? p.score : p.kv) + src, (uint32_t)d * 2u, &full[s]);
+        // tiles (tensor t, window half h, column box cb): [R tokens x bx columns]
+        for (int j = lane % g; j < 2 * COFF * ncb; j += g) {
+          const int t = j & 1, h = (j >> 1) % COFF, cb = (j >> 1) / COFF;
+          if (COFF == 2 && h == 0 && first) continue;  // masked previous block
+          const int y = (int)(COFF == 2 && h == 0 ? base - R : base);
+          const int x = h * d + cb * bx;
+          uint16_t* dst = stages + s * stage_elems + my_row * row_elems +
+                          ((int64_t)(t * COFF + h) * ncb + cb) * R * bx;
+          tma_load_2d(dst, t ? &tm_sc : &tm_kv, x, y, &full[s]);
         }
       }
     }
@@ -276,7 +283,9 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
       if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
         st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
       } else {
-        const uint16_t* src = stages + s * stage_elems + r * row_elems + j0;
+        // slot k = (half h, token k mod R) of column box j0 / bx
+        const uint16_t* src = stages + s * stage_elems + r * row_elems +
+                              (int64_t)(j0 / bx) * R * bx + (j0 % bx);
         uint4 kvv[W], scv[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
@@ -284,8 +293,10 @@ fwd_small_pc_kernel(const FwdParams f, int ns) {
             kvv[k] = make_uint4(0u, 0u, 0u, 0u);
             scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
           } else {
-            kvv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)k * d);
-            scv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)(W + k) * d);
+            const int h = k / R, tk = k % R;
+            const int64_t o = ((int64_t)h * ncb * R + tk) * bx;
+            kvv[k] = *reinterpret_cast<const uint4*>(src + o);
+            scv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)COFF * ncb * R * bx + o);
           }
         }
         uint32_t ow[4];
@@ -469,20 +480,27 @@ cudaError_t launch_small_pc(const FwdParams& f, cudaStream_t stream, bool* launc
   constexpr int W = COFF * R;
   *launched = false;
   const int d = f.p.d;
-  if (!CSA_FWD_PC || d < 256 || d > 2048 || f.p.C == 0) return cudaSuccess;
+  if (!CSA_FWD_PC || d < 256 || d > 2048 || d % 256 != 0 || f.p.C == 0 || f.p.T < R)
+    return cudaSuccess;
   const int rs = kPcConsumers / (d / kVec);
   const size_t stage_bytes = (size_t)rs * 2 * W * d * 2;
   int ns = (int)(kPcRingBytes / stage_bytes);
   if (ns > 8) ns = 8;
   if (ns < 2) return cudaSuccess;
-  const size_t smem = (size_t)ns * stage_bytes + 2 * (size_t)ns * sizeof(uint64_t);
+  const size_t smem = (size_t)ns * stage_bytes + 2 * (size_t)ns * sizeof(uint64_t) + 128;
+  const int bx = 256;
+  const uint64_t ld = (uint64_t)COFF * d;
+  CUtensorMap tm_kv, tm_sc;
+  cudaError_t e = encode_bf16_rows(&tm_kv, f.p.kv, ld, (uint64_t)f.p.T, bx, R);
+  if (e == cudaSuccess) e = encode_bf16_rows(&tm_sc, f.p.score, ld, (uint64_t)f.p.T, bx, R);
+  if (e != cudaSuccess) return cudaSuccess;  // no tensor maps here: the register kernel runs instead
   auto kern = fwd_small_pc_kernel<R, COFF>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nchunks = (f.p.C + rs - 1) / rs;
   int64_t grid = sm_count();
   if (grid > nchunks) grid = nchunks;
-  kern<<<(unsigned)grid, kPcThreads, smem, stream>>>(f, ns);
+  kern<<<(unsigned)grid, kPcThreads, smem, stream>>>(f, ns, tm_kv, tm_sc, bx);
   *launched = true;
   return cudaGetLastError();
 }
