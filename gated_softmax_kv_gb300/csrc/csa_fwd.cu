@@ -139,14 +139,15 @@ fwd_small_kernel(const FwdParams f) {
 // of shared-memory stages with 2D tensor-map copies (TMA engine): per tensor
 // and window half, tiles of [ratio tokens x 256 columns] (2 KB at ratio 4;
 // 1 KB pieces measured well below the 2 KB rate on this GPU), counted on a
-// per-stage "full" mbarrier. Eight consumer warps compute the rows of a
-// stage from shared memory (a thread owns 8 columns of one row, its APE
+// per-stage "full" mbarrier. Sixteen consumer warps compute the rows of a
+// stage from shared memory (a thread owns 4 columns of one row, its APE
 // columns in registers) and release the stage on its "empty" mbarrier. The
 // loads of the next stages stay in flight while the current one is computed.
 // Same arithmetic as fwd_small_kernel. Chunk q of rows [q rs, q rs + rs) goes
 // to CTA q mod gridDim.x.
-constexpr int kPcConsumers = 256;               // 8 consumer warps
+constexpr int kPcConsumers = 512;               // 16 consumer warps
 constexpr int kPcThreads = kPcConsumers + 32;   // + 1 producer warp
+constexpr int kPcVc = 4;                        // columns per consumer thread
 constexpr size_t kPcRingBytes = 192 * 1024;     // shared-memory budget of the stage ring
 
 #ifndef CSA_FWD_PC
@@ -163,7 +164,7 @@ fwd_small_pc_kernel(const FwdParams f, int ns, const __grid_constant__ CUtensorM
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
   const int d = p.d;
-  const int txc = d / kVec;            // consumer threads per row
+  const int txc = d / kPcVc;           // consumer threads per row
   const int rs = kPcConsumers / txc;   // rows per chunk (<= 8)
   const int64_t ld = (int64_t)COFF * d;
   const int ncb = d / bx;  // column boxes per window half
@@ -254,22 +255,16 @@ fwd_small_pc_kernel(const FwdParams f, int ns, const __grid_constant__ CUtensorM
     return;
   }
 
-  // consumers: thread (r, tx) owns columns 8 tx .. 8 tx + 7 of row r of each chunk
+  // consumers: thread (r, tx) owns columns 4 tx .. 4 tx + 3 of row r of each chunk
   const int r = tid / txc, tx = tid - (tid / txc) * txc;
   const bool active = r < rs;
-  const int j0 = tx * kVec;
-  float apev[W][kVec];
+  const int j0 = tx * kPcVc;
+  float apev[W][kPcVc];
 #pragma unroll
   for (int k = 0; k < W; ++k) {
-    if (active) {
-      const float* a = p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + j0;
-      const float4 lo = ld_f4(a), hi = ld_f4(a + 4);
-      apev[k][0] = lo.x; apev[k][1] = lo.y; apev[k][2] = lo.z; apev[k][3] = lo.w;
-      apev[k][4] = hi.x; apev[k][5] = hi.y; apev[k][6] = hi.z; apev[k][7] = hi.w;
-    } else {
-#pragma unroll
-      for (int c = 0; c < kVec; ++c) apev[k][c] = 0.0f;
-    }
+    const float4 a = active ? ld_f4(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + j0)
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    apev[k][0] = a.x; apev[k][1] = a.y; apev[k][2] = a.z; apev[k][3] = a.w;
   }
   int hint = 0;
   int64_t n = 0;
@@ -281,49 +276,44 @@ fwd_small_pc_kernel(const FwdParams f, int ns, const __grid_constant__ CUtensorM
       const RowInfo ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
       uint16_t* dst = f.out + b * d + j0;
       if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
-        st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
+        st_stream8(dst, make_uint2(0x7FC07FC0u, 0x7FC07FC0u));
       } else {
         // slot k = (half h, token k mod R) of column box j0 / bx
         const uint16_t* src = stages + s * stage_elems + r * row_elems +
                               (int64_t)(j0 / bx) * R * bx + (j0 % bx);
-        uint4 kvv[W], scv[W];
+        uint2 kvv[W], scv[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           if (S::masked(ri.first, k)) {
-            kvv[k] = make_uint4(0u, 0u, 0u, 0u);
-            scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+            kvv[k] = make_uint2(0u, 0u);
+            scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
           } else {
             const int h = k / R, tk = k % R;
             const int64_t o = ((int64_t)h * ncb * R + tk) * bx;
-            kvv[k] = *reinterpret_cast<const uint4*>(src + o);
-            scv[k] = *reinterpret_cast<const uint4*>(src + (int64_t)COFF * ncb * R * bx + o);
+            kvv[k] = *reinterpret_cast<const uint2*>(src + o);
+            scv[k] = *reinterpret_cast<const uint2*>(src + (int64_t)COFF * ncb * R * bx + o);
           }
         }
-        uint32_t ow[4];
+        float res[kPcVc];
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
-          float res[2];
+        for (int c = 0; c < kPcVc; ++c) {
+          float z[W];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 2 * c2 + h;
-            float z[W];
+          for (int k = 0; k < W; ++k)
+            z[k] = __fadd_rn(bf16_at(c < 2 ? scv[k].x : scv[k].y, c & 1), apev[k][c]);
+          float m = z[0];
 #pragma unroll
-            for (int k = 0; k < W; ++k) z[k] = __fadd_rn(bf16_elem(scv[k], c), apev[k][c]);
-            float m = z[0];
+          for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
+          float den = 0.0f, acc = 0.0f;
 #pragma unroll
-            for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
-            float den = 0.0f, acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-              const float e = softmax_exp(__fsub_rn(z[k], m));
-              den = __fadd_rn(den, e);
-              acc = __fmaf_rn(e, bf16_elem(kvv[k], c), acc);
-            }
-            res[h] = __fdiv_rn(acc, den);
+          for (int k = 0; k < W; ++k) {
+            const float e = softmax_exp(__fsub_rn(z[k], m));
+            den = __fadd_rn(den, e);
+            acc = __fmaf_rn(e, bf16_at(c < 2 ? kvv[k].x : kvv[k].y, c & 1), acc);
           }
-          ow[c2] = pack_bf16x2(res[0], res[1]);
+          res[c] = __fdiv_rn(acc, den);
         }
-        st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+        st_stream8(dst, make_uint2(pack_bf16x2(res[0], res[1]), pack_bf16x2(res[2], res[3])));
       }
     }
     __syncwarp();
@@ -482,7 +472,7 @@ cudaError_t launch_small_pc(const FwdParams& f, cudaStream_t stream, bool* launc
   const int d = f.p.d;
   if (!CSA_FWD_PC || d < 256 || d > 2048 || d % 256 != 0 || f.p.C == 0 || f.p.T < R)
     return cudaSuccess;
-  const int rs = kPcConsumers / (d / kVec);
+  const int rs = kPcConsumers / (d / kPcVc);
   const size_t stage_bytes = (size_t)rs * 2 * W * d * 2;
   int ns = (int)(kPcRingBytes / stage_bytes);
   if (ns > 8) ns = 8;
