@@ -5,10 +5,8 @@ as hand-written CUDA kernels behind a small C ABI (include/csa_compress.h);
 this package holds the kernels (csrc/), their build and a thin Python binding.
 """
 from .binding import (CsaError, csa_compress_bwd, csa_compress_bwd_noalloc_ptr,
-                      csa_compress_bwd_ptr, csa_compress_fwd, csa_compress_fwd_ptr, load,
-                      read_device_faults)
+                      csa_compress_bwd_ptr, csa_compress_fwd, csa_compress_fwd_ptr, load)
 from .nvbuild import build
 
 __all__ = ["CsaError", "build", "csa_compress_bwd", "csa_compress_bwd_noalloc_ptr",
-           "csa_compress_bwd_ptr", "csa_compress_fwd", "csa_compress_fwd_ptr", "load",
-           "read_device_faults"]
+           "csa_compress_bwd_ptr", "csa_compress_fwd", "csa_compress_fwd_ptr", "load"]

@@ -192,18 +192,3 @@ def csa_compress_bwd_noalloc_ptr(kv: int, score: int, ape: int, cu_seqlens: int,
             coff, head_dim, grad_out, dkv, dscore, dape, stream)
     if st != 0:
         _raise(st)
-
-
-def read_device_faults() -> int:
-    """Read and clear the current device's fault word (synchronous): bit 0 set
-    means a bounded wait in a kernel gave up since the last read."""
-    lib = load()
-    fn = lib.csa_read_device_faults
-    if fn.argtypes is None:
-        fn.argtypes = [ctypes.c_void_p]
-        fn.restype = ctypes.c_int
-    flags = ctypes.c_int32(0)
-    st = fn(ctypes.byref(flags))
-    if st != 0:
-        _raise(st)
-    return int(flags.value)

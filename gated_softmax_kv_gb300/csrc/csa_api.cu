@@ -129,9 +129,7 @@ csa_status_t csa_compress_fwd(const void* kv, const void* score, const float* ap
   f.p = make_problem(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
                      capacity, ratio, coff, head_dim);
   f.out = static_cast<uint16_t*>(out);
-  cudaError_t e = csa::device_fault_word(&f.faults);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = csa::launch_fwd(f, stream);
+  cudaError_t e = csa::launch_fwd(f, stream);
   return e == cudaSuccess ? CSA_OK : cuda_fail(e);
 }
 

@@ -32,28 +32,12 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-
-// 1: the small-window backward stages each thread's next row through shared
-// memory with cp.async (bwd_small_pipe_kernel); 0: plain register loads.
-#ifndef CSA_BWD_SMALL_PIPE
-#define CSA_BWD_SMALL_PIPE 0
-#endif
 constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
 
 
 // Zeros for the positions no row reads that belong to nobody's window:
 // segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
 // Spread over every CTA of the launch.
-__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) {
-  const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
   const Problem& p = bp.p;
   const int64_t ld = (int64_t)p.coff * p.d;
@@ -242,216 +226,6 @@ bwd_small_kernel(const BwdParams bp) {
       }
     }
   }
-
-  zero_orphans(bp, R);
-
-  // combine the TY thread rows in ascending order, then write this CTA's
-  // slice of the partial of row group blockIdx.y
-  __syncthreads();
-  for (int t = 0; t < TY; ++t) {
-    if (ty == t && col_ok) {
-#pragma unroll
-      for (int k = 0; k < W; ++k)
-#pragma unroll
-        for (int c = 0; c < kCv; ++c) {
-          float* s = sm + k * tile_cols + tx * kCv + c;
-          *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
-        }
-    }
-    __syncthreads();
-  }
-  float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
-  for (int i = tid; i < W * tile_cols; i += nthr) {
-    const int k = i / tile_cols;
-    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    if (col < d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = sm[i];
-  }
-}
-
-// Same thread mapping and arithmetic as bwd_small_kernel, with the loads
-// decoupled from the registers: each thread copies its next row's window
-// (cp.async, 8-byte pieces) into its own slots of a two-stage shared-memory
-// buffer while it computes the current row from the other stage.
-template <int R, int COFF, int D>
-__global__ void __launch_bounds__(kThreads, 2)
-bwd_small_pipe_kernel(const BwdParams bp) {
-  constexpr int W = COFF * R;
-  using S = Slot<R, COFF>;
-  const Problem& p = bp.p;
-  const int d = D > 0 ? D : p.d;
-  const int TX = blockDim.x, TY = blockDim.y;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  const int tid = ty * TX + tx, nthr = TX * TY;
-  const int ncv = d / kCv;
-  const int cv = blockIdx.x * TX + tx;
-  const bool col_ok = cv < ncv;
-  const int64_t ld = (int64_t)COFF * d;
-  const int j0 = cv * kCv;
-  const int tile_cols = TX * kCv;
-  // element offset of slot k from (row base token, column j0)
-  auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
-
-  // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
-  extern __shared__ float sm[];
-  for (int i = tid; i < W * tile_cols; i += nthr) {
-    const int k = i / tile_cols;
-    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
-  }
-  __syncthreads();
-  const float* ape_s = sm + tx * kCv;
-
-  float dacc[W][kCv];
-#pragma unroll
-  for (int k = 0; k < W; ++k)
-#pragma unroll
-    for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
-
-  const uint2 zero2 = make_uint2(0u, 0u);
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  const int64_t stride = (int64_t)gridDim.y * TY;
-  // stage s, entry e (slot k: 2k kv, 2k+1 score; 2W grad_out) of this thread
-  constexpr int NE = 2 * W + 1;
-  uint2* stages = reinterpret_cast<uint2*>(sm + W * tile_cols);
-  auto entry = [&](int s, int e) { return stages + ((int64_t)s * NE + e) * nthr + tid; };
-  int hint_issue = 0, hint = 0;
-  auto issue = [&](int64_t b, int s) {
-    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint_issue);
-    if (!row_in_bounds<R, COFF>(ri, p.T) || b >= p.C) return;
-    const int64_t rowoff = ri.base * ld + j0;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      if (S::masked(ri.first, k)) continue;
-      cp_async8(entry(s, 2 * k), p.kv + rowoff + koff(k));
-      cp_async8(entry(s, 2 * k + 1), p.score + rowoff + koff(k));
-    }
-    cp_async8(entry(s, 2 * W), bp.grad_out + b * d + j0);
-  };
-  int64_t b = (int64_t)blockIdx.y * TY + ty;
-  if (col_ok && b < true_rows) issue(b, 0);
-  cp_async_commit();
-  for (int it = 0; col_ok && b < true_rows; ++it, b += stride) {
-    if (b + stride < true_rows) issue(b + stride, (it + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();  // this row's pieces have landed
-    const int st = it & 1;
-    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
-    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
-    const int64_t rowoff = ri.base * ld + j0;
-    uint16_t* dkv_row = bp.dkv + rowoff;
-    uint16_t* dsc_row = bp.dscore + rowoff;
-    if (b < p.C) {
-      uint2 kvv[W], scv[W];
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) {
-          kvv[k] = zero2;
-          scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
-        } else {
-          kvv[k] = *entry(st, 2 * k);
-          scv[k] = *entry(st, 2 * k + 1);
-        }
-      }
-      const uint2 gv = *entry(st, 2 * W);
-
-      // z = score + ape, then in place e = exp(z - m), then p = e / den
-      float pz[W][kCv];
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
-        pz[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
-        pz[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
-        pz[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
-        pz[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
-      }
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        // both columns of the pair: m, e, den, p, then S
-        float sum[2], g[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * c2 + h;
-          float m = pz[0][c];
-#pragma unroll
-          for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
-          float den = 0.0f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            pz[k][c] = softmax_exp(__fsub_rn(pz[k][c], m));
-            den = __fadd_rn(den, pz[k][c]);
-          }
-          const float y = __frcp_rn(den);
-#pragma unroll
-          for (int k = 0; k < W; ++k) pz[k][c] = div_rn_by_rcp(pz[k][c], den, y);
-          g[h] = bf16_at(c2 ? gv.y : gv.x, h);
-          float acc = 0.0f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
-            acc = __fadd_rn(acc, __fmul_rn(dp, pz[k][c]));
-          }
-          sum[h] = acc;
-        }
-        // dscore = p (dp - S), dkv = g p, packed per slot as soon as both columns exist;
-        // the packed words reuse the raw score registers, which are dead by now
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          float dz[2], dk[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 2 * c2 + h;
-            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
-            dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
-            dk[h] = __fmul_rn(g[h], pz[k][c]);
-            dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);
-          }
-          if (c2 == 0) {
-            scv[k].x = pack_bf16x2(dz[0], dz[1]);
-            kvv[k].x = pack_bf16x2(dk[0], dk[1]);
-          } else {
-            scv[k].y = pack_bf16x2(dz[0], dz[1]);
-            kvv[k].y = pack_bf16x2(dk[0], dk[1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) continue;
-        st_stream8(dkv_row + koff(k), kvv[k]);
-        st_stream8(dsc_row + koff(k), scv[k]);
-      }
-    } else {
-      // a row past capacity has no output slot: zero gradient at its positions
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) continue;
-        st_stream8(dkv_row + koff(k), zero2);
-        st_stream8(dsc_row + koff(k), zero2);
-      }
-    }
-    if (ri.last) {
-      // the segment's last row owns its block's unread first-half columns ...
-      if (COFF == 2) {
-#pragma unroll
-        for (int t = 0; t < R; ++t) {
-          st_stream8(dkv_row + t * ld, zero2);
-          st_stream8(dsc_row + t * ld, zero2);
-        }
-      }
-      // ... and the segment's tail tokens (seqlen % ratio of them)
-      const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
-      for (int64_t tok = ri.base + R; tok < tail_end; ++tok) {
-#pragma unroll
-        for (int h = 0; h < COFF; ++h) {
-          const int64_t off = tok * ld + h * d + j0;
-          st_stream8(bp.dkv + off, zero2);
-          st_stream8(bp.dscore + off, zero2);
-        }
-      }
-    }
-  }
-
-  cp_async_wait<0>();
 
   zero_orphans(bp, R);
 
@@ -776,9 +550,8 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const int tx = ncv <= 128 ? ncv : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kCv +
-                      (CSA_BWD_SMALL_PIPE ? sizeof(uint2) * 2 * (2 * W + 1) * tx * ty : 0);
-  auto kern = CSA_BWD_SMALL_PIPE ? bwd_small_pipe_kernel<R, COFF, D> : bwd_small_kernel<R, COFF, D>;
+  const size_t smem = sizeof(float) * W * tx * kCv;
+  auto kern = bwd_small_kernel<R, COFF, D>;
   static bool attr = [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
     return true;
@@ -830,21 +603,12 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
 
 template <int R, int COFF>
 cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  if (CSA_BWD_SMALL_PIPE) {
-    if (b.p.d == 512)
-      bwd_small_pipe_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
-    else if (b.p.d == 128)
-      bwd_small_pipe_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
-    else
-      bwd_small_pipe_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
-  } else {
-    if (b.p.d == 512)
-      bwd_small_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
-    else if (b.p.d == 128)
-      bwd_small_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
-    else
-      bwd_small_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
-  }
+  if (b.p.d == 512)
+    bwd_small_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
+  else if (b.p.d == 128)
+    bwd_small_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
+  else
+    bwd_small_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
   return cudaGetLastError();
 }
 

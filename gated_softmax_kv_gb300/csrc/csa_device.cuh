@@ -187,39 +187,6 @@ __device__ __forceinline__ RowInfo row_info_from(const int32_t* __restrict__ cu,
   return ri;
 }
 
-// row_info_from on segment arrays in any address space (plain loads; used
-// with copies of cu_seqlens / cu_seqlens_comp staged in shared memory).
-__device__ __forceinline__ RowInfo row_info_any(const int32_t* cu, const int32_t* cuc, int nseq,
-                                                int64_t b, int64_t true_rows, int ratio, int& hint) {
-  RowInfo ri;
-  if (b >= true_rows) {
-    ri.base = 0;
-    ri.seg_end = 0;
-    ri.first = true;
-    ri.last = false;
-    return ri;
-  }
-  int lo = hint;
-  int64_t c1 = cuc[lo + 1];
-  if (c1 <= b) {
-    int hi = nseq;
-    lo = lo + 1;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if ((int64_t)cuc[mid] <= b) lo = mid; else hi = mid;
-    }
-    c1 = cuc[lo + 1];
-  }
-  hint = lo;
-  const int64_t c0 = cuc[lo];
-  const int64_t i = b - c0;
-  ri.base = (int64_t)cu[lo] + i * ratio;
-  ri.seg_end = cu[lo + 1];
-  ri.first = (i == 0);
-  ri.last = (i == c1 - c0 - 1);
-  return ri;
-}
-
 // Window slot k of a row: token offset from base, column offset (0 or d),
 // APE row; masked when it is a previous-block slot of a first block.
 template <int R, int COFF>

@@ -28,7 +28,6 @@
 
 #include <mutex>
 
-#include "csa_async.cuh"
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -131,193 +130,6 @@ fwd_small_kernel(const FwdParams f) {
       ow[c2] = pack_bf16x2(res[0], res[1]);
     }
     st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
-  }
-}
-
-// Producer/consumer forward (W <= 8, 256 <= head_dim <= 2048, head_dim a
-// multiple of 256). One producer warp streams each row's window into a ring
-// of shared-memory stages with 2D tensor-map copies (TMA engine): per tensor
-// and window half, tiles of [ratio tokens x 256 columns] (2 KB at ratio 4;
-// 1 KB pieces measured well below the 2 KB rate on this GPU), counted on a
-// per-stage "full" mbarrier. Sixteen consumer warps compute the rows of a
-// stage from shared memory (a thread owns 4 columns of one row, its APE
-// columns in registers) and release the stage on its "empty" mbarrier. The
-// loads of the next stages stay in flight while the current one is computed.
-// Same arithmetic as fwd_small_kernel. Chunk q of rows [q rs, q rs + rs) goes
-// to CTA q mod gridDim.x.
-constexpr int kPcConsumers = 512;               // 16 consumer warps
-constexpr int kPcThreads = kPcConsumers + 32;   // + 1 producer warp
-constexpr int kPcVc = 4;                        // columns per consumer thread
-constexpr size_t kPcRingBytes = 192 * 1024;     // shared-memory budget of the stage ring
-
-#ifndef CSA_FWD_PC
-#define CSA_FWD_PC 1
-#endif
-
-constexpr int kPcSegCache = 2048;  // segment-array entries staged in shared memory
-
-template <int R, int COFF>
-__global__ void __launch_bounds__(kPcThreads, 1)
-fwd_small_pc_kernel(const FwdParams f, int ns, const __grid_constant__ CUtensorMap tm_kv,
-                    const __grid_constant__ CUtensorMap tm_sc, int bx) {
-  constexpr int W = COFF * R;
-  using S = Slot<R, COFF>;
-  const Problem& p = f.p;
-  const int d = p.d;
-  const int txc = d / kPcVc;           // consumer threads per row
-  const int rs = kPcConsumers / txc;   // rows per chunk (<= 8)
-  const int64_t ld = (int64_t)COFF * d;
-  const int ncb = d / bx;  // column boxes per window half
-  // row layout: [kv | score][window half g][column box][token of the block][bx]
-  const int64_t row_elems = (int64_t)2 * W * d;
-  const int64_t stage_elems = row_elems * rs;
-  const uint32_t box_bytes = (uint32_t)R * (uint32_t)bx * 2u;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  // tiles land 128-byte aligned (the launch adds 128 bytes of slack)
-  uint8_t* smem_al = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint16_t* stages = reinterpret_cast<uint16_t*>(smem_al);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_al + (size_t)ns * stage_elems * 2);
-  uint64_t* empty = full + ns;
-  __shared__ int32_t cu_s[kPcSegCache], cuc_s[kPcSegCache];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t nchunks = (p.C + rs - 1) / rs;
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  // segment arrays: staged in shared memory when they fit (row lookups then
-  // cost no global round trip), else read from global memory
-  const bool seg_cached = p.nseq + 1 <= kPcSegCache;
-  if (seg_cached) {
-    for (int i = tid; i <= p.nseq; i += kPcThreads) {
-      cu_s[i] = __ldg(p.cu + i);
-      cuc_s[i] = __ldg(p.cuc + i);
-    }
-  }
-  const int32_t* cu = seg_cached ? cu_s : p.cu;
-  const int32_t* cuc = seg_cached ? cuc_s : p.cuc;
-
-  if (tid == 0) {
-    for (int s = 0; s < ns; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kPcConsumers / 32);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  if (warp == kPcConsumers / 32) {
-    // producer: lane r (< rs) looks up row r of each chunk; all 32 lanes share
-    // the 2W copies per row
-    int hint = 0;
-    int64_t n = 0;
-    for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++n) {
-      const int s = (int)(n % ns);
-      const uint32_t use = (uint32_t)(n / ns);
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, f.faults)) break;
-      const int64_t b = q * rs + lane;
-      bool fetch = false;
-      RowInfo ri;
-      ri.base = 0;
-      ri.first = true;
-      uint32_t bytes = 0;
-      if (lane < rs && b < p.C) {
-        ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
-        fetch = row_in_bounds<R, COFF>(ri, p.T);
-        if (fetch)  // both tensors, every column box, of each loaded window half
-          bytes = (uint32_t)(COFF == 2 && ri.first ? 1 : COFF) * (uint32_t)ncb * 2u * box_bytes;
-      }
-      uint32_t total = bytes;
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
-      __syncwarp();
-      // lanes [r g, r g + g) copy the 2W pieces of row r (g = 32 / rs lanes per row)
-      const int g = 32 / rs;
-      const int my_row = lane / g < rs ? lane / g : 0;
-      const int64_t base = __shfl_sync(0xffffffffu, ri.base, my_row);
-      const int first = __shfl_sync(0xffffffffu, (int)ri.first, my_row);
-      const int ok = __shfl_sync(0xffffffffu, (int)fetch, my_row);
-      if (lane / g < rs && ok) {
-        // tiles (tensor t, window half h, column box cb): [R tokens x bx columns]
-        for (int j = lane % g; j < 2 * COFF * ncb; j += g) {
-          const int t = j & 1, h = (j >> 1) % COFF, cb = (j >> 1) / COFF;
-          if (COFF == 2 && h == 0 && first) continue;  // masked previous block
-          const int y = (int)(COFF == 2 && h == 0 ? base - R : base);
-          const int x = h * d + cb * bx;
-          uint16_t* dst = stages + s * stage_elems + my_row * row_elems +
-                          ((int64_t)(t * COFF + h) * ncb + cb) * R * bx;
-          tma_load_2d(dst, t ? &tm_sc : &tm_kv, x, y, &full[s]);
-        }
-      }
-    }
-    // no copy into this CTA's shared memory may be in flight when it exits:
-    // wait for the last fill of every stage (bounded)
-    for (int64_t m = n > ns ? n - ns : 0; m < n; ++m)
-      mbar_wait(&full[m % ns], (uint32_t)(m / ns) & 1u, f.faults);
-    return;
-  }
-
-  // consumers: thread (r, tx) owns columns 4 tx .. 4 tx + 3 of row r of each chunk
-  const int r = tid / txc, tx = tid - (tid / txc) * txc;
-  const bool active = r < rs;
-  const int j0 = tx * kPcVc;
-  float apev[W][kPcVc];
-#pragma unroll
-  for (int k = 0; k < W; ++k) {
-    const float4 a = active ? ld_f4(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + j0)
-                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    apev[k][0] = a.x; apev[k][1] = a.y; apev[k][2] = a.z; apev[k][3] = a.w;
-  }
-  int hint = 0;
-  int64_t n = 0;
-  for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++n) {
-    const int s = (int)(n % ns);
-    if (!mbar_wait(&full[s], (uint32_t)(n / ns) & 1u, f.faults)) break;
-    const int64_t b = q * rs + r;
-    if (active && b < p.C) {
-      const RowInfo ri = row_info_any(cu, cuc, p.nseq, b, true_rows, R, hint);
-      uint16_t* dst = f.out + b * d + j0;
-      if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
-        st_stream8(dst, make_uint2(0x7FC07FC0u, 0x7FC07FC0u));
-      } else {
-        // slot k = (half h, token k mod R) of column box j0 / bx
-        const uint16_t* src = stages + s * stage_elems + r * row_elems +
-                              (int64_t)(j0 / bx) * R * bx + (j0 % bx);
-        uint2 kvv[W], scv[W];
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          if (S::masked(ri.first, k)) {
-            kvv[k] = make_uint2(0u, 0u);
-            scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
-          } else {
-            const int h = k / R, tk = k % R;
-            const int64_t o = ((int64_t)h * ncb * R + tk) * bx;
-            kvv[k] = *reinterpret_cast<const uint2*>(src + o);
-            scv[k] = *reinterpret_cast<const uint2*>(src + (int64_t)COFF * ncb * R * bx + o);
-          }
-        }
-        float res[kPcVc];
-#pragma unroll
-        for (int c = 0; c < kPcVc; ++c) {
-          float z[W];
-#pragma unroll
-          for (int k = 0; k < W; ++k)
-            z[k] = __fadd_rn(bf16_at(c < 2 ? scv[k].x : scv[k].y, c & 1), apev[k][c]);
-          float m = z[0];
-#pragma unroll
-          for (int k = 1; k < W; ++k) m = max_nan(m, z[k]);
-          float den = 0.0f, acc = 0.0f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const float e = softmax_exp(__fsub_rn(z[k], m));
-            den = __fadd_rn(den, e);
-            acc = __fmaf_rn(e, bf16_at(c < 2 ? kvv[k].x : kvv[k].y, c & 1), acc);
-          }
-          res[c] = __fdiv_rn(acc, den);
-        }
-        st_stream8(dst, make_uint2(pack_bf16x2(res[0], res[1]), pack_bf16x2(res[2], res[3])));
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -466,40 +278,7 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
 }
 
 template <int R, int COFF>
-cudaError_t launch_small_pc(const FwdParams& f, cudaStream_t stream, bool* launched) {
-  constexpr int W = COFF * R;
-  *launched = false;
-  const int d = f.p.d;
-  if (!CSA_FWD_PC || d < 256 || d > 2048 || d % 256 != 0 || f.p.C == 0 || f.p.T < R)
-    return cudaSuccess;
-  const int rs = kPcConsumers / (d / kPcVc);
-  const size_t stage_bytes = (size_t)rs * 2 * W * d * 2;
-  int ns = (int)(kPcRingBytes / stage_bytes);
-  if (ns > 8) ns = 8;
-  if (ns < 2) return cudaSuccess;
-  const size_t smem = (size_t)ns * stage_bytes + 2 * (size_t)ns * sizeof(uint64_t) + 128;
-  const int bx = 256;
-  const uint64_t ld = (uint64_t)COFF * d;
-  CUtensorMap tm_kv, tm_sc;
-  cudaError_t e = encode_bf16_rows(&tm_kv, f.p.kv, ld, (uint64_t)f.p.T, bx, R);
-  if (e == cudaSuccess) e = encode_bf16_rows(&tm_sc, f.p.score, ld, (uint64_t)f.p.T, bx, R);
-  if (e != cudaSuccess) return cudaSuccess;  // no tensor maps here: the register kernel runs instead
-  auto kern = fwd_small_pc_kernel<R, COFF>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int64_t nchunks = (f.p.C + rs - 1) / rs;
-  int64_t grid = sm_count();
-  if (grid > nchunks) grid = nchunks;
-  kern<<<(unsigned)grid, kPcThreads, smem, stream>>>(f, ns, tm_kv, tm_sc, bx);
-  *launched = true;
-  return cudaGetLastError();
-}
-
-template <int R, int COFF>
 cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
-  bool launched = false;
-  cudaError_t e = launch_small_pc<R, COFF>(f, stream, &launched);
-  if (e != cudaSuccess || launched) return e;
   if (f.p.d == 512) return launch_small_d<R, COFF, 512>(f, stream);
   if (f.p.d == 128) return launch_small_d<R, COFF, 128>(f, stream);
   return launch_small_d<R, COFF, 0>(f, stream);

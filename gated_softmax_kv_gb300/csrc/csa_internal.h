@@ -2,7 +2,6 @@
 // translation units (csa_fwd.cu, csa_bwd.cu). Not installed, not part of the ABI.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,7 +26,6 @@ struct Problem {
 struct FwdParams {
   Problem p;
   uint16_t* out;           // [C, d]
-  unsigned int* faults;    // device fault word (bounded waits that gave up)
 };
 
 struct BwdParams {
@@ -58,14 +56,6 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
-
-// Device address of the fault word on the current device (csa_async.cu).
-cudaError_t device_fault_word(unsigned int** out);
-
-// Tensor map of a row-major [rows, cols] bf16 tensor with box [box_rows, box_cols]
-// (csa_async.cu; cuTensorMapEncodeTiled through the runtime's driver entry point).
-cudaError_t encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                             uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace csa
 

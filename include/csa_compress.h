@@ -139,16 +139,6 @@ csa_status_t csa_compress_bwd_noalloc(const void* kv, const void* score, const f
                                       const void* grad_out, void* dkv, void* dscore, float* dape,
                                       cudaStream_t stream);
 
-/*
- * Reads and clears the current device's fault word (synchronous: it waits for
- * the device). Some kernels wait on hardware barriers for their own
- * asynchronous copies; each such wait is bounded (one second), and a wait that
- * gives up sets bit 0 (1 = a bounded wait gave up) and leaves that call's
- * outputs unspecified instead of hanging. 0 means no fault since the last read.
- * This is a diagnostic of this library, not an operation of the paper.
- */
-csa_status_t csa_read_device_faults(int32_t* flags);
-
 /* Static description of a status code (never null). */
 const char* csa_status_string(csa_status_t status);
 
