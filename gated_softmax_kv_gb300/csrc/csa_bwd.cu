@@ -38,17 +38,6 @@ constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte ve
 // Zeros for the positions no row reads that belong to nobody's window:
 // segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
 // Spread over every CTA of the launch.
-template <int BYTES>
-__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src) {
-  const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(gmem_src), "n"(BYTES) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
   const Problem& p = bp.p;
   const int64_t ld = (int64_t)p.coff * p.d;
@@ -363,58 +352,24 @@ bwd_long_kernel(const BwdParams bp) {
   // merge thread layout: column mc of the tile, group member mq (G per column)
   const int mc = tid / G, mq = tid % G;
 
-  // The next row's window pieces of this thread travel to its own slots of a
-  // two-stage shared-memory ring (cp.async) while the current row is reduced.
-  using VT = typename V::T;
-  constexpr int NE = 2 * KPT + 1;  // kv slots, score slots, grad_out
-  extern __shared__ __align__(16) unsigned char lw_ring[];
-  VT* ring = reinterpret_cast<VT*>(lw_ring);
-  auto ent = [&](int st, int e) -> VT* { return ring + ((int64_t)st * NE + e) * NT + tid; };
-  auto issue = [&](int64_t bb, const RowInfo& rj, int st) {
-    if (!col_ok || bb >= p.C || !row_in_bounds<R, COFF>(rj, p.T)) return;
-    if (!S::masked(rj.first, k0)) {
-      const int64_t o = rj.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
-#pragma unroll
-      for (int t = 0; t < KPT; ++t) {
-        cp_async<sizeof(VT)>(ent(st, t), p.kv + o + t * ld);
-        cp_async<sizeof(VT)>(ent(st, KPT + t), p.score + o + t * ld);
-      }
-    }
-    cp_async<sizeof(VT)>(ent(st, 2 * KPT), bp.grad_out + bb * d + j0);
-  };
-
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  RowInfo ri_next;
-  if ((int64_t)blockIdx.y < true_rows) {
-    ri_next = row_info(p.cu, p.cuc, p.nseq, blockIdx.y, true_rows, R);
-    issue(blockIdx.y, ri_next, 0);
-  }
-  cp_async_commit();
-  int it = 0;
-  for (int64_t b = blockIdx.y; b < true_rows; b += gridDim.y, ++it) {
-    const RowInfo ri = ri_next;
-    if (b + gridDim.y < true_rows) {
-      ri_next = row_info(p.cu, p.cuc, p.nseq, b + gridDim.y, true_rows, R);
-      issue(b + gridDim.y, ri_next, (it + 1) & 1);
-    }
-    cp_async_commit();
-    cp_async_wait<1>();  // this row's pieces have landed in stage it & 1
-    const int st = it & 1;
+  for (int64_t b = blockIdx.y; b < true_rows; b += gridDim.y) {
+    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
     if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // uniform over the CTA
     const bool chunk_masked = S::masked(ri.first, k0);
     const bool active = col_ok && !chunk_masked;
     const int64_t off = ri.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
     if (b < p.C) {
       // phase 1
-      VT kvw[KPT], scw[KPT];
+      typename V::T kvw[KPT], scw[KPT];
 #pragma unroll
       for (int t = 0; t < KPT; ++t) {
-        kvw[t] = active ? *ent(st, t) : V::zero();
-        scw[t] = active ? *ent(st, KPT + t) : V::ninf();
+        kvw[t] = active ? V::load(p.kv + off + t * ld) : V::zero();
+        scw[t] = active ? V::load(p.score + off + t * ld) : V::ninf();
       }
       float g[VC];
       {
-        const VT gw = col_ok ? *ent(st, 2 * KPT) : V::zero();
+        const typename V::T gw = col_ok ? V::load(bp.grad_out + b * d + j0) : V::zero();
 #pragma unroll
         for (int c = 0; c < VC; ++c) g[c] = V::elem(gw, c);
       }
@@ -543,8 +498,6 @@ bwd_long_kernel(const BwdParams bp) {
     }
   }
 
-  cp_async_wait<0>();
-
   zero_orphans(bp, R);
 
   // each (slot, column) of the tile belongs to exactly one thread
@@ -630,14 +583,8 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
   constexpr int NT = LongShape<W>::kThreads;
   const int ncv = p.d / LongShape<W>::kVc;
   const int tiles = (ncv + 31) / 32;
-  const size_t smem = (size_t)2 * (2 * LongShape<W>::kKpt + 1) * NT * 2 * LongShape<W>::kVc;
   auto kern = bwd_long_kernel<R, COFF>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    return true;
-  }();
-  (void)attr;
-  const int occ = occupancy(kern, NT, smem);
+  const int occ = occupancy(kern, NT, 0);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy > p.C) gy = p.C;
   if (gy < 1) gy = 1;
@@ -649,7 +596,7 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
   if (gy > 65535) gy = 65535;
   s->grid = dim3(tiles, (unsigned)gy);
   s->block = dim3(32, LongShape<W>::kNch);
-  s->smem = smem;
+  s->smem = 0;
   s->groups = (int32_t)gy;
   return cudaSuccess;
 }
