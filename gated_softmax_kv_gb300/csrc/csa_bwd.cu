@@ -32,6 +32,12 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
+
+// Long-window backward: windows of at least this many slots give each warp 16
+// slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
+#ifndef CSA_BWD_LONG_KPT16_FROM
+#define CSA_BWD_LONG_KPT16_FROM 128
+#endif
 constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
 
 
@@ -269,8 +275,8 @@ bwd_small_kernel(const BwdParams bp) {
 //            registers (each thread owns its KPT slots x VC columns)
 template <int W>
 struct LongShape {
-  static constexpr int kKpt = W >= 256 ? 16 : 8;             // slots per warp
-  static constexpr int kVc = (W >= 256 || W <= 16) ? 2 : 4;  // columns per lane
+  static constexpr int kKpt = W >= CSA_BWD_LONG_KPT16_FROM ? 16 : 8;                   // slots per warp
+  static constexpr int kVc = (W >= CSA_BWD_LONG_KPT16_FROM || W <= 16) ? 2 : 4;        // columns per lane
   static constexpr int kNch = W / kKpt;                      // warps per CTA
   static constexpr int kThreads = 32 * kNch;
   static constexpr int kMinBlocks = kThreads >= 512 ? 1 : 512 / kThreads;  // <= 128 registers
