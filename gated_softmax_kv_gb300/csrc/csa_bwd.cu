@@ -36,7 +36,7 @@ constexpr int kThreads = 256;
 // Long-window backward: windows of at least this many slots give each warp 16
 // slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
 #ifndef CSA_BWD_LONG_KPT16_FROM
-#define CSA_BWD_LONG_KPT16_FROM 128
+#define CSA_BWD_LONG_KPT16_FROM 256
 #endif
 constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
 
