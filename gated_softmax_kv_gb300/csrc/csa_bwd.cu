@@ -14,7 +14,7 @@
 // dape is reduced deterministically in two levels, without atomics: each CTA
 // accumulates its rows' logit gradients in registers (rows in a fixed order),
 // combines its threads in a fixed order and writes one fp32 partial per row
-// group; dape_reduce then sums the partials in group order and overwrites dape.
+// group; dape_reduce then sums the partials in a fixed order and overwrites dape.
 //
 // Kernel shapes mirror the forward (csa_fwd.cu): bwd_small keeps a W <= 8
 // window of 4 columns per thread in registers and follows the plain eager
@@ -518,24 +518,35 @@ bwd_long_kernel(const BwdParams bp) {
   }
 }
 
-// dape[e] = sum over groups g (ascending) of partial[g][e], in two fixed
-// levels: 16 lanes take every 16th group in order, then lane 0 adds the 16
-// lane sums in order.
-__global__ void __launch_bounds__(512)
+// dape[e] = sum over groups g of partial[g][e] in two fixed levels: lane y of
+// 32 sums groups y, y + 32, y + 64, ... in ascending order (loads issued 8
+// at a time so they overlap), then lane 0 adds the 32 lane sums in order.
+constexpr int kReduceLanes = 32;
+
+__global__ void __launch_bounds__(32 * kReduceLanes)
 dape_reduce_kernel(const float* __restrict__ partial, int32_t groups, int64_t n,
                    float* __restrict__ dape) {
-  __shared__ float red[16][33];
+  __shared__ float red[kReduceLanes][33];
   const int64_t e = (int64_t)blockIdx.x * 32 + threadIdx.x;
   float s = 0.0f;
   if (e < n) {
-#pragma unroll 4
-    for (int g = threadIdx.y; g < groups; g += 16) s = __fadd_rn(s, __ldcs(partial + (int64_t)g * n + e));
+    for (int g0 = threadIdx.y; g0 < groups; g0 += 8 * kReduceLanes) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = g0 + i * kReduceLanes;
+        v[i] = g < groups ? __ldcs(partial + (int64_t)g * n + e) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (g0 + i * kReduceLanes < groups) s = __fadd_rn(s, v[i]);
+    }
   }
   red[threadIdx.y][threadIdx.x] = s;
   __syncthreads();
   if (threadIdx.y == 0 && e < n) {
     float t = red[0][threadIdx.x];
-    for (int y = 1; y < 16; ++y) t = __fadd_rn(t, red[y][threadIdx.x]);
+    for (int y = 1; y < kReduceLanes; ++y) t = __fadd_rn(t, red[y][threadIdx.x]);
     dape[e] = t;
   }
 }
@@ -658,7 +669,7 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
                                cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   const int64_t blocks = (n + 31) / 32;
-  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, 16), 0, stream>>>(partial, groups, n, dape);
+  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, kReduceLanes), 0, stream>>>(partial, groups, n, dape);
   return cudaGetLastError();
 }
 
