@@ -37,6 +37,11 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// exp of the small-window forward (see softmax_exp)
+#ifndef CSA_FWD_EXP
+#define CSA_FWD_EXP softmax_exp
+#endif
+
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
 // D == 0 reads it from the problem.
 template <int R, int COFF, int D>
@@ -121,7 +126,7 @@ fwd_small_kernel(const FwdParams f) {
         float den = 0.0f, acc = 0.0f;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          const float e = softmax_exp(__fsub_rn(z[k][c], m));
+          const float e = CSA_FWD_EXP(__fsub_rn(z[k][c], m));
           den = __fadd_rn(den, e);
           acc = __fmaf_rn(e, bf16_elem(kvv[k], c), acc);
         }
