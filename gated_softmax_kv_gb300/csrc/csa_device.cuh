@@ -72,8 +72,9 @@ __device__ __forceinline__ float softmax_exp(float x) {
   return __fmaf_rn(r, __fmul_rn(err, kLn2), r);
 }
 
-// 2^(x log2 e) with a single rounding of the product (no error term): about
-// |x| 2^-24 relative error from the product plus the ex2.approx error.
+// exp(x) as 2^(x log2 e) with a single rounding of the product (no error
+// term): relative error about |x| 2^-24 from the product plus that of
+// ex2.approx. Clamp and NaN handling as softmax_exp.
 __device__ __forceinline__ float softmax_exp_fast(float x) {
   x = max_nan(x, -100.0f);
   return ex2_approx_ftz(__fmul_rn(x, __int_as_float(0x3fb8aa3b)));

@@ -37,9 +37,13 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// exp of the small-window forward (see softmax_exp)
+// exp of the forward kernels. The forward has no bitwise target (the page's
+// numerics give it "one bf16 rounding step on a tiny fraction of elements"),
+// so it uses the single-rounding softmax_exp_fast: 5.6% faster at the
+// headline with the differing count unchanged within noise. The backward keeps
+// the compensated softmax_exp.
 #ifndef CSA_FWD_EXP
-#define CSA_FWD_EXP softmax_exp
+#define CSA_FWD_EXP softmax_exp_fast
 #endif
 
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
@@ -222,12 +226,12 @@ fwd_long_kernel(const FwdParams f) {
         for (int t = 0; t < kBatch; ++t) mn = max_nan(mn, z[t][c]);
         // while every logit so far is -inf, shift by 0 so exp gives 0, not NaN
         const float mu = mn == kNegInf ? 0.0f : mn;
-        const float alpha = softmax_exp(__fsub_rn(m[c], mu));
+        const float alpha = CSA_FWD_EXP(__fsub_rn(m[c], mu));
         float dn = __fmul_rn(den[c], alpha);
         float ac = __fmul_rn(acc[c], alpha);
 #pragma unroll
         for (int t = 0; t < kBatch; ++t) {
-          const float e = softmax_exp(__fsub_rn(z[t][c], mu));
+          const float e = CSA_FWD_EXP(__fsub_rn(z[t][c], mu));
           dn = __fadd_rn(dn, e);
           ac = __fmaf_rn(e, bf16_at(c < 2 ? kvb[t].x : kvb[t].y, c & 1), ac);
         }

@@ -86,3 +86,36 @@ def test_division_from_reciprocal_is_correctly_rounded():
     bad = np.nonzero(normal & (got.view(np.uint32) != want.view(np.uint32)))[0]
     detail = [(float(a[i]), float(b[i]), float(got[i]), float(want[i])) for i in bad[:8]]
     assert bad.size == 0, f"{bad.size} quotients differ (a, b, got, want): {detail}"
+
+
+def test_forward_fast_exp_error_bound():
+    """The forward's single-rounding exp: relative error within (|x| + 4) * 2^-24
+    of the correctly rounded exp on [-87, 0] (the product x * log2 e is rounded
+    once, ex2.approx adds a few units of 2^-24)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    lib.csa_selftest_softmax_exp_fast.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                  ctypes.c_void_p]
+    lib.csa_selftest_softmax_exp_fast.restype = ctypes.c_int32
+    lo, hi = np.float32(-87.0).view(np.uint32), np.uint32(0x80000000)
+    xs = np.arange(hi, lo, 64, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    xs = np.concatenate([xs, np.linspace(-1.0, 0.0, 1 << 20, dtype=np.float32)])
+    x_d = torch.from_numpy(xs).cuda()
+    y_d = torch.empty_like(x_d)
+    assert lib.csa_selftest_softmax_exp_fast(x_d.data_ptr(), y_d.data_ptr(), xs.size, None) == 0
+    torch.cuda.synchronize()
+    got = y_d.cpu().numpy().astype(np.float64)
+    want = oracle.exp_f32_array(xs).astype(np.float64)
+    normal = want >= 2.0 ** -126
+    rel = np.abs(got[normal] - want[normal]) / want[normal]
+    bound = (np.abs(xs[normal].astype(np.float64)) + 4.0) * 2.0 ** -24
+    print("max rel err", float(rel.max()), "max rel / bound", float((rel / bound).max()))
+    assert np.all(rel <= bound)
+    sp = torch.tensor([float("-inf"), float("nan")], device="cuda")
+    out = torch.empty_like(sp)
+    assert lib.csa_selftest_softmax_exp_fast(sp.data_ptr(), out.data_ptr(), 2, None) == 0
+    o = out.cpu().numpy()
+    assert o[0] == 0.0 and np.isnan(o[1])
