@@ -89,9 +89,12 @@ def test_division_from_reciprocal_is_correctly_rounded():
 
 
 def test_forward_fast_exp_error_bound():
-    """The forward's single-rounding exp: relative error within (|x| + 4) * 2^-24
-    of the correctly rounded exp on [-87, 0] (the product x * log2 e is rounded
-    once, ex2.approx adds a few units of 2^-24)."""
+    """The forward's single-rounding exp against the correctly rounded exp on
+    [-87, 0]. Error budget: fp32(log2 e) is off by 1.34e-8 relative and the
+    product x * fp32(log2 e) is rounded once (<= 2^-24 relative), which gives
+    2^t a relative error of at most ln 2 * |x| log2 e * (1.34e-8 + 2^-24)
+    = 1.23 |x| 2^-24; ex2.approx and the final rounding add a few units of
+    2^-24. Bound used: (1.25 |x| + 8) * 2^-24."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from gated_softmax_kv_gb300 import nvbuild
@@ -111,7 +114,7 @@ def test_forward_fast_exp_error_bound():
     want = oracle.exp_f32_array(xs).astype(np.float64)
     normal = want >= 2.0 ** -126
     rel = np.abs(got[normal] - want[normal]) / want[normal]
-    bound = (np.abs(xs[normal].astype(np.float64)) + 4.0) * 2.0 ** -24
+    bound = (1.25 * np.abs(xs[normal].astype(np.float64)) + 8.0) * 2.0 ** -24
     print("max rel err", float(rel.max()), "max rel / bound", float((rel / bound).max()))
     assert np.all(rel <= bound)
     sp = torch.tensor([float("-inf"), float("nan")], device="cuda")
