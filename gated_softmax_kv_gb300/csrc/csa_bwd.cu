@@ -264,15 +264,16 @@ bwd_small_kernel(const BwdParams bp) {
 // (32 VC)-column tile (blockIdx.x), so every load and store of a warp covers
 // 32 VC * 2 contiguous bytes of one token row. The CTA walks rows
 // b = blockIdx.y, blockIdx.y + gridDim.y, ... and per row:
-//   phase 1  z = score + ape, the chunk's max m_c and e = exp(z - m_c), sum e
-//   merge    (max, sum) of the NCH chunks of a column, in a fixed order:
+//   phase 1  z = score + ape, the chunk's max m_c, e = exp(z - m_c), sum e and
+//            T_c = sum (g kv) e
+//   merge    (max, sum, T) of the NCH chunks of a column, in a fixed order:
 //            NCH/VC threads take VC chunks each, then a butterfly over those
-//            lanes (commutative combines, so every lane gets the same bits)
+//            lanes (commutative combines, so every lane gets the same bits);
+//            S = sum (g kv) p = T / den
 //   phase 2  p = e * exp(m_c - M) / den (one exp and one reciprocal per column
-//            and chunk), the chunk's share of S = sum (g kv) p
-//   merge    S the same way
-//   phase 3  dscore = p (g kv - S), dkv = g p, stores; dape accumulates in
-//            registers (each thread owns its KPT slots x VC columns)
+//            and chunk), dscore = p (g kv - S), dkv = g p, stores; dape
+//            accumulates in registers (each thread owns KPT slots x VC columns)
+// Two barriers per row.
 template <int W>
 struct LongShape {
   static constexpr int kKpt = W >= CSA_BWD_LONG_KPT16_FROM ? 16 : 8;                   // slots per warp
@@ -308,13 +309,17 @@ struct ColVec<4> {
   }
 };
 
-// fixed-order merge of (max, sum exp) pairs: m = max, s = s_a e^(m_a - m) + s_b e^(m_b - m)
-__device__ __forceinline__ void merge_max_sum(float& m, float& s, float mb, float sb) {
+// fixed-order merge of (max, sum exp, sum (g kv) exp) triples rescaled to the
+// common max: m = max, s = s_a e^(m_a - m) + s_b e^(m_b - m), t likewise.
+// Symmetric in a and b, so both lanes of a butterfly step get the same bits.
+__device__ __forceinline__ void merge_max_sum2(float& m, float& s, float& t, float mb, float sb,
+                                               float tb) {
   const float kNegInf = __int_as_float(0xff800000);
   const float mn = max_nan(m, mb);
   const float mu = mn == kNegInf ? 0.0f : mn;
-  s = __fadd_rn(__fmul_rn(s, softmax_exp(__fsub_rn(m, mu))),
-                __fmul_rn(sb, softmax_exp(__fsub_rn(mb, mu))));
+  const float fa = softmax_exp(__fsub_rn(m, mu)), fb = softmax_exp(__fsub_rn(mb, mu));
+  s = __fadd_rn(__fmul_rn(s, fa), __fmul_rn(sb, fb));
+  t = __fadd_rn(__fmul_rn(t, fa), __fmul_rn(tb, fb));
   m = mn;
 }
 
@@ -390,6 +395,9 @@ bwd_long_kernel(const BwdParams bp) {
           pz[t][c + 1] = __fadd_rn(V::elem(scw[t], c + 1), a.y);
         }
       }
+      // phase 1: per column, the chunk's max m_c, e = exp(z - m_c), its sum
+      // and T_c = sum (g kv) e; one fixed-order merge of (max, sum, T) then
+      // gives the row's max M, den and S = T / den together
       float mloc[VC];
 #pragma unroll
       for (int c = 0; c < VC; ++c) {
@@ -397,33 +405,38 @@ bwd_long_kernel(const BwdParams bp) {
 #pragma unroll
         for (int t = 1; t < KPT; ++t) m = max_nan(m, pz[t][c]);
         const float mu = m == kNegInf ? 0.0f : m;  // an all -inf chunk contributes 0
-        float sum = 0.0f;
+        float sum = 0.0f, tsum = 0.0f;
 #pragma unroll
         for (int t = 0; t < KPT; ++t) {
           pz[t][c] = softmax_exp(__fsub_rn(pz[t][c], mu));
           sum = __fadd_rn(sum, pz[t][c]);
+          tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c]));
         }
         mloc[c] = m;
         m_s[y * LDS + lane * VC + c] = m;
         d_s[y * LDS + lane * VC + c] = sum;
+        s_s[y * LDS + lane * VC + c] = tsum;
       }
       __syncthreads();
       {
         float m = m_s[(mq * VC) * LDS + mc], sm = d_s[(mq * VC) * LDS + mc];
+        float tm = s_s[(mq * VC) * LDS + mc];
 #pragma unroll
         for (int i = 1; i < VC; ++i)
-          merge_max_sum(m, sm, m_s[(mq * VC + i) * LDS + mc], d_s[(mq * VC + i) * LDS + mc]);
+          merge_max_sum2(m, sm, tm, m_s[(mq * VC + i) * LDS + mc], d_s[(mq * VC + i) * LDS + mc],
+                         s_s[(mq * VC + i) * LDS + mc]);
 #pragma unroll
         for (int mask = 1; mask < G; mask <<= 1)
-          merge_max_sum(m, sm, __shfl_xor_sync(0xffffffffu, m, mask),
-                        __shfl_xor_sync(0xffffffffu, sm, mask));
+          merge_max_sum2(m, sm, tm, __shfl_xor_sync(0xffffffffu, m, mask),
+                         __shfl_xor_sync(0xffffffffu, sm, mask), __shfl_xor_sync(0xffffffffu, tm, mask));
         if (mq == 0) {
           M_s[mc] = m;
           D_s[mc] = sm;
+          S_s[mc] = __fdiv_rn(tm, sm);
         }
       }
       __syncthreads();
-      // phase 2
+      // phase 2: p = e exp(m_c - M) / den, dscore = p (g kv - S), dkv = g p
 #pragma unroll
       for (int c = 0; c < VC; ++c) {
         const float M = M_s[lane * VC + c];
@@ -432,26 +445,9 @@ bwd_long_kernel(const BwdParams bp) {
         const float ml = mloc[c] == kNegInf ? 0.0f : mloc[c];
         const float f = softmax_exp(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
         const float yr = __frcp_rn(den);
-        float acc = 0.0f;
 #pragma unroll
-        for (int t = 0; t < KPT; ++t) {
-          pz[t][c] = div_rn_by_rcp(__fmul_rn(pz[t][c], f), den, yr);
-          const float dp = __fmul_rn(g[c], V::elem(kvw[t], c));
-          acc = __fadd_rn(acc, __fmul_rn(dp, pz[t][c]));
-        }
-        s_s[y * LDS + lane * VC + c] = acc;
+        for (int t = 0; t < KPT; ++t) pz[t][c] = div_rn_by_rcp(__fmul_rn(pz[t][c], f), den, yr);
       }
-      __syncthreads();
-      {
-        float sm = s_s[(mq * VC) * LDS + mc];
-#pragma unroll
-        for (int i = 1; i < VC; ++i) sm = __fadd_rn(sm, s_s[(mq * VC + i) * LDS + mc]);
-#pragma unroll
-        for (int mask = 1; mask < G; mask <<= 1) sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, mask));
-        if (mq == 0) S_s[mc] = sm;
-      }
-      __syncthreads();
-      // phase 3
       float Sv[VC];
 #pragma unroll
       for (int c = 0; c < VC; ++c) Sv[c] = S_s[lane * VC + c];
