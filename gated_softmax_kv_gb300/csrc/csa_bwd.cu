@@ -351,15 +351,8 @@ bwd_long_kernel(const BwdParams bp) {
   __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
   __shared__ float M_s[TC], D_s[TC], S_s[TC];
 
-  // the CTA's APE tile, [W slots][TC columns], staged once in shared memory
-  extern __shared__ __align__(16) float ape_tile[];
-  for (int i = tid; i < W * TC; i += NT) {
-    const int k = i / TC;
-    const int col = blockIdx.x * TC + (i - k * TC);
-    ape_tile[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
-  }
-  __syncthreads();
-  const float* ape_t = ape_tile + k0 * TC + lane * VC;  // slot k0 + t at ape_t[t * TC]
+  // this thread's APE values (slots k0.., columns j0..) are re-read per row through L1
+  const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
 
   float dacc[KPT][VC];
 #pragma unroll
@@ -396,7 +389,8 @@ bwd_long_kernel(const BwdParams bp) {
       for (int t = 0; t < KPT; ++t) {
 #pragma unroll
         for (int c = 0; c < VC; c += 2) {
-          const float2 a = *reinterpret_cast<const float2*>(ape_t + t * TC + c);
+          const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld + c))
+                                  : make_float2(0.0f, 0.0f);
           pz[t][c] = __fadd_rn(V::elem(scw[t], c), a.x);
           pz[t][c + 1] = __fadd_rn(V::elem(scw[t], c + 1), a.y);
         }
@@ -602,14 +596,8 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
   constexpr int NT = LongShape<W>::kThreads;
   const int ncv = p.d / LongShape<W>::kVc;
   const int tiles = (ncv + 31) / 32;
-  const size_t smem = sizeof(float) * (size_t)W * 32 * LongShape<W>::kVc;  // APE tile
   auto kern = bwd_long_kernel<R, COFF>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    return true;
-  }();
-  (void)attr;
-  const int occ = occupancy(kern, NT, smem);
+  const int occ = occupancy(kern, NT, 0);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy > p.C) gy = p.C;
   if (gy < 1) gy = 1;
@@ -621,7 +609,7 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
   if (gy > 65535) gy = 65535;
   s->grid = dim3(tiles, (unsigned)gy);
   s->block = dim3(32, LongShape<W>::kNch);
-  s->smem = smem;
+  s->smem = 0;
   s->groups = (int32_t)gy;
   return cudaSuccess;
 }
