@@ -237,4 +237,19 @@ def config(name: str, seed: int = 0, fill: bool = True) -> Case:
     if name == "headline":
         return make_case(name, headline_seqlens(seed), 4, 2, 512, pad_rows=1024, seed=seed,
                          fill=fill)
+    if name.startswith("pack-"):
+        return pack(name, seed=seed, fill=fill)
     raise KeyError(name)
+
+
+def pack(spec: str, seed: int = 0, fill: bool = True) -> Case:
+    """A THD pack of equal segments, spelt `pack-r{ratio}c{coff}d{head_dim}-{n}x{len}`
+    (e.g. `pack-r4c2d128-3x8192`): the segment counts and lengths at which the
+    cuDNN-frontend "CSA Fused Compressor" page quotes its kernel times; no
+    padding rows, the page's gate distribution."""
+    import re
+    m = re.fullmatch(r"pack-r(\d+)c([12])d(\d+)-(\d+)x(\d+)", spec)
+    if m is None:
+        raise KeyError(spec)
+    r, coff, d, n, length = (int(x) for x in m.groups())
+    return make_case(spec, [length] * n, r, coff, d, seed=seed, fill=fill)
