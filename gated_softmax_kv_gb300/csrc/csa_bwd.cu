@@ -514,35 +514,55 @@ bwd_long_kernel(const BwdParams bp) {
   }
 }
 
-// dape[e] = sum over groups g of partial[g][e] in two fixed levels: lane y of
-// 32 sums groups y, y + 32, y + 64, ... in ascending order (loads issued 8
-// at a time so they overlap), then lane 0 adds the 32 lane sums in order.
-constexpr int kReduceLanes = 32;
+// dape[e] = sum over groups g of partial[g][e] in two fixed levels. A lane
+// owns 4 consecutive elements (16-byte loads; every group row starts on a
+// 32-byte boundary because ratio * coff * d is a multiple of 8). Lane y of the
+// blockDim.y lanes that share those elements sums groups y, y + Y, y + 2Y, ...
+// in ascending order (loads issued 8 at a time so they overlap), then lane 0
+// adds the Y lane sums in order. Y (a power of two <= 32) is fixed by the
+// launch from n and groups, so the order is the same on every run.
+constexpr int kReduceMaxLanes = 32;
 
-__global__ void __launch_bounds__(32 * kReduceLanes)
-dape_reduce_kernel(const float* __restrict__ partial, int32_t groups, int64_t n,
-                   float* __restrict__ dape) {
-  __shared__ float red[kReduceLanes][33];
+__global__ void __launch_bounds__(32 * kReduceMaxLanes)
+dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n4,
+                   float4* __restrict__ dape) {
+  __shared__ float4 red[kReduceMaxLanes][32];
+  const int Y = blockDim.y;
   const int64_t e = (int64_t)blockIdx.x * 32 + threadIdx.x;
-  float s = 0.0f;
-  if (e < n) {
-    for (int g0 = threadIdx.y; g0 < groups; g0 += 8 * kReduceLanes) {
-      float v[8];
+  float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (e < n4) {
+    for (int g0 = threadIdx.y; g0 < groups; g0 += 8 * Y) {
+      float4 v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int g = g0 + i * kReduceLanes;
-        v[i] = g < groups ? __ldcs(partial + (int64_t)g * n + e) : 0.0f;
+        const int g = g0 + i * Y;
+        v[i] = g < groups ? __ldcs(partial + (int64_t)g * n4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (g0 + i * kReduceLanes < groups) s = __fadd_rn(s, v[i]);
+        if (g0 + i * Y < groups) {
+          s.x = __fadd_rn(s.x, v[i].x);
+          s.y = __fadd_rn(s.y, v[i].y);
+          s.z = __fadd_rn(s.z, v[i].z);
+          s.w = __fadd_rn(s.w, v[i].w);
+        }
     }
+  }
+  if (Y == 1) {
+    if (e < n4) dape[e] = s;
+    return;
   }
   red[threadIdx.y][threadIdx.x] = s;
   __syncthreads();
-  if (threadIdx.y == 0 && e < n) {
-    float t = red[0][threadIdx.x];
-    for (int y = 1; y < kReduceLanes; ++y) t = __fadd_rn(t, red[y][threadIdx.x]);
+  if (threadIdx.y == 0 && e < n4) {
+    float4 t = red[0][threadIdx.x];
+    for (int y = 1; y < Y; ++y) {
+      const float4 u = red[y][threadIdx.x];
+      t.x = __fadd_rn(t.x, u.x);
+      t.y = __fadd_rn(t.y, u.y);
+      t.z = __fadd_rn(t.z, u.z);
+      t.w = __fadd_rn(t.w, u.w);
+    }
     dape[e] = t;
   }
 }
@@ -664,8 +684,17 @@ cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t s
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
                                cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  const int64_t blocks = (n + 31) / 32;
-  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, kReduceLanes), 0, stream>>>(partial, groups, n, dape);
+  const int64_t n4 = n / 4;  // n = ratio * coff * d, a multiple of 8
+  const int64_t blocks = (n4 + 31) / 32;
+  // lanes per element group: about two waves of 2048-thread SMs over the
+  // whole GPU, at most one lane per partial; a constant of the problem (152 is
+  // the SM count of a GB300, fixed here so that the order does not depend on
+  // the device)
+  int lanes = 1;
+  while (lanes < kReduceMaxLanes && lanes * 2 <= groups && blocks * 32 * lanes * 2 <= 2 * 152 * 2048)
+    lanes *= 2;
+  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, lanes), 0, stream>>>(
+      reinterpret_cast<const float4*>(partial), groups, n4, reinterpret_cast<float4*>(dape));
   return cudaGetLastError();
 }
 

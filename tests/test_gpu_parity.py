@@ -181,3 +181,14 @@ def test_zero_capacity():
     dc = _dev(case)
     dkv, ds, dape = dc.bwd(prefill=0x7FC0)
     assert np.all(dkv == 0) and np.all(ds == 0) and np.all(dape == 0)
+
+
+@pytest.mark.parametrize("name", ["pack-r128c2d128-1x65536", "pack-r128c1d512-1x65536",
+                                  "pack-r4c2d128-1x8192"])
+def test_parity_page_packs(name):
+    """Single-sequence packs at the sizes the page quotes kernel times for; with
+    few output rows the long-window forward splits each window over several
+    warps and merges the chunk states."""
+    res = check_case(workloads.config(name))
+    print(name, {k: (v if not isinstance(v, dict) else (v["differing"], v["max_abs"]))
+                 for k, v in res.items()})
