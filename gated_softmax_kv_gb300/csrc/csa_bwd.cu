@@ -33,6 +33,12 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// exp of the long-window backward's per-element weights. Windows of 16 slots
+// and more have no bitwise target (the page aims at bit identity for ratios 2
+// and 4 only), so they take the single-rounding softmax_exp_fast.
+#ifndef CSA_BWD_LONG_EXP
+#define CSA_BWD_LONG_EXP softmax_exp_fast
+#endif
 // Long-window backward: windows of at least this many slots give each warp 16
 // slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
 #ifndef CSA_BWD_LONG_KPT16_FROM
@@ -270,10 +276,14 @@ bwd_small_kernel(const BwdParams bp) {
 //            NCH/VC threads take VC chunks each, then a butterfly over those
 //            lanes (commutative combines, so every lane gets the same bits);
 //            S = sum (g kv) p = T / den
-//   phase 2  p = e * exp(m_c - M) / den (one exp and one reciprocal per column
-//            and chunk), dscore = p (g kv - S), dkv = g p, stores; dape
-//            accumulates in registers (each thread owns KPT slots x VC columns)
-// Two barriers per row.
+//   phase 2  p = e * (exp(m_c - M) / den) (one exp and one reciprocal per
+//            column and chunk), dscore = p (g kv - S), dkv = g p, stores; dape
+//            accumulates in shared memory (each thread owns KPT slots x VC
+//            columns of the [W][TC] table, so no barrier guards it)
+// Two barriers per row. The next row's kv, score and grad_out loads are
+// issued before the merge, so they are in flight through the merge and
+// phase 2 (one CTA of NCH warps per SM would otherwise leave HBM idle while
+// it computes).
 template <int W>
 struct LongShape {
   static constexpr int kKpt = W >= CSA_BWD_LONG_KPT16_FROM ? 16 : 8;                   // slots per warp
@@ -323,7 +333,9 @@ __device__ __forceinline__ void merge_max_sum2(float& m, float& s, float& t, flo
   m = mn;
 }
 
-template <int R, int COFF>
+// D > 0 fixes head_dim at compile time (slot offsets become immediates);
+// D == 0 reads it from the problem.
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(LongShape<COFF * R>::kThreads, LongShape<COFF * R>::kMinBlocks)
 bwd_long_kernel(const BwdParams bp) {
   constexpr int W = COFF * R;
@@ -337,7 +349,7 @@ bwd_long_kernel(const BwdParams bp) {
   using S = Slot<R, COFF>;
   using V = ColVec<VC>;
   const Problem& p = bp.p;
-  const int d = p.d;
+  const int d = D > 0 ? D : p.d;
   const int lane = threadIdx.x, y = threadIdx.y;
   const int tid = y * 32 + lane;
   const int ncv = d / VC;
@@ -350,41 +362,60 @@ bwd_long_kernel(const BwdParams bp) {
 
   __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
   __shared__ float M_s[TC], D_s[TC], S_s[TC];
+  // dape sums of the tile, [W][TC]; each cell belongs to one thread
+  extern __shared__ float dacc_s[];
+  float* dacc_t = dacc_s + k0 * TC + lane * VC;
+#pragma unroll
+  for (int t = 0; t < KPT; ++t)
+#pragma unroll
+    for (int c = 0; c < VC; ++c) dacc_t[t * TC + c] = 0.0f;
 
   // this thread's APE values (slots k0.., columns j0..) are re-read per row through L1
   const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
 
-  float dacc[KPT][VC];
-#pragma unroll
-  for (int t = 0; t < KPT; ++t)
-#pragma unroll
-    for (int c = 0; c < VC; ++c) dacc[t][c] = 0.0f;
-
   // merge thread layout: column mc of the tile, group member mq (G per column)
   const int mc = tid / G, mq = tid % G;
 
+  // The next row's kv, score and grad_out are loaded while the current row
+  // merges and runs phase 2 (score into the registers phase 1 has consumed).
+  typename V::T kvw[KPT], scw[KPT], gw = V::zero();
+  auto offset = [&](const RowInfo& r) {
+    return r.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
+  };
+  auto loads = [&](int64_t rb, const RowInfo& r, typename V::T (&kvb)[KPT], typename V::T& gb) {
+    // rows past capacity and rows that break the preconditions load nothing
+    if (rb >= p.C || !row_in_bounds<R, COFF>(r, p.T)) {
+#pragma unroll
+      for (int t = 0; t < KPT; ++t) kvb[t] = V::zero();
+      return;
+    }
+    const bool act = col_ok && !S::masked(r.first, k0);
+    const int64_t off = offset(r);
+#pragma unroll
+    for (int t = 0; t < KPT; ++t) {
+      kvb[t] = act ? V::load(p.kv + off + t * ld) : V::zero();
+      scw[t] = act ? V::load(p.score + off + t * ld) : V::ninf();
+    }
+    gb = col_ok ? V::load(bp.grad_out + rb * d + j0) : V::zero();
+  };
+
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  for (int64_t b = blockIdx.y; b < true_rows; b += gridDim.y) {
-    const RowInfo ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
-    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // uniform over the CTA
-    const bool chunk_masked = S::masked(ri.first, k0);
-    const bool active = col_ok && !chunk_masked;
-    const int64_t off = ri.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
-    if (b < p.C) {
-      // phase 1
-      typename V::T kvw[KPT], scw[KPT];
+  int64_t b = blockIdx.y;
+  RowInfo ri{};
+  if (b < true_rows) {
+    ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    loads(b, ri, kvw, gw);
+  }
+  for (; b < true_rows;) {
+    const bool row_ok = row_in_bounds<R, COFF>(ri, p.T);  // uniform over the CTA
+    const bool active = col_ok && !S::masked(ri.first, k0);
+    const int64_t off = offset(ri);
+    const bool compute = row_ok && b < p.C;  // uniform over the CTA
+    float g[VC], mloc[VC];
+    float pz[KPT][VC];
+    if (compute) {
 #pragma unroll
-      for (int t = 0; t < KPT; ++t) {
-        kvw[t] = active ? V::load(p.kv + off + t * ld) : V::zero();
-        scw[t] = active ? V::load(p.score + off + t * ld) : V::ninf();
-      }
-      float g[VC];
-      {
-        const typename V::T gw = col_ok ? V::load(bp.grad_out + b * d + j0) : V::zero();
-#pragma unroll
-        for (int c = 0; c < VC; ++c) g[c] = V::elem(gw, c);
-      }
-      float pz[KPT][VC];
+      for (int c = 0; c < VC; ++c) g[c] = V::elem(gw, c);
 #pragma unroll
       for (int t = 0; t < KPT; ++t) {
 #pragma unroll
@@ -398,7 +429,6 @@ bwd_long_kernel(const BwdParams bp) {
       // phase 1: per column, the chunk's max m_c, e = exp(z - m_c), its sum
       // and T_c = sum (g kv) e; one fixed-order merge of (max, sum, T) then
       // gives the row's max M, den and S = T / den together
-      float mloc[VC];
 #pragma unroll
       for (int c = 0; c < VC; ++c) {
         float m = pz[0][c];
@@ -408,7 +438,7 @@ bwd_long_kernel(const BwdParams bp) {
         float sum = 0.0f, tsum = 0.0f;
 #pragma unroll
         for (int t = 0; t < KPT; ++t) {
-          pz[t][c] = softmax_exp(__fsub_rn(pz[t][c], mu));
+          pz[t][c] = CSA_BWD_LONG_EXP(__fsub_rn(pz[t][c], mu));
           sum = __fadd_rn(sum, pz[t][c]);
           tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c]));
         }
@@ -417,6 +447,16 @@ bwd_long_kernel(const BwdParams bp) {
         d_s[y * LDS + lane * VC + c] = sum;
         s_s[y * LDS + lane * VC + c] = tsum;
       }
+    }
+    // prefetch the next row of this CTA
+    const int64_t bn = b + gridDim.y;
+    RowInfo rn{};
+    typename V::T kvn[KPT], gn = V::zero();
+    if (bn < true_rows) {
+      rn = row_info(p.cu, p.cuc, p.nseq, bn, true_rows, R);
+      loads(bn, rn, kvn, gn);
+    }
+    if (compute) {
       __syncthreads();
       {
         float m = m_s[(mq * VC) * LDS + mc], sm = d_s[(mq * VC) * LDS + mc];
@@ -444,9 +484,11 @@ bwd_long_kernel(const BwdParams bp) {
         const float mu = M == kNegInf ? 0.0f : M;
         const float ml = mloc[c] == kNegInf ? 0.0f : mloc[c];
         const float f = softmax_exp(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
-        const float yr = __frcp_rn(den);
+        // one scale per column and chunk: f / den (no per-element division;
+        // like the exp above, not correctly rounded)
+        const float fy = __fmul_rn(f, __frcp_rn(den));
 #pragma unroll
-        for (int t = 0; t < KPT; ++t) pz[t][c] = div_rn_by_rcp(__fmul_rn(pz[t][c], f), den, yr);
+        for (int t = 0; t < KPT; ++t) pz[t][c] = __fmul_rn(pz[t][c], fy);
       }
       float Sv[VC];
 #pragma unroll
@@ -458,14 +500,14 @@ bwd_long_kernel(const BwdParams bp) {
         for (int c = 0; c < VC; ++c) {
           dz[c] = __fmul_rn(pz[t][c], __fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]));
           dk[c] = __fmul_rn(g[c], pz[t][c]);
-          dacc[t][c] = __fadd_rn(dacc[t][c], dz[c]);
+          dacc_t[t * TC + c] = __fadd_rn(dacc_t[t * TC + c], dz[c]);
         }
         if (active) {
           V::store(bp.dkv + off + t * ld, V::pack(dk));
           V::store(bp.dscore + off + t * ld, V::pack(dz));
         }
       }
-    } else if (active) {
+    } else if (row_ok && active) {
       // a row past capacity has no output slot: zero gradient at its positions
 #pragma unroll
       for (int t = 0; t < KPT; ++t) {
@@ -473,7 +515,7 @@ bwd_long_kernel(const BwdParams bp) {
         V::store(bp.dscore + off + t * ld, V::zero());
       }
     }
-    if (ri.last) {
+    if (row_ok && ri.last) {
       // unread positions owned by the segment's last row, for this column tile:
       // its block's first-half columns (coff 2) and the segment tail
       const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
@@ -498,6 +540,11 @@ bwd_long_kernel(const BwdParams bp) {
         V::store(bp.dscore + tok * ld + h * d + col_v * VC, V::zero());
       }
     }
+    b = bn;
+    ri = rn;
+    gw = gn;
+#pragma unroll
+    for (int t = 0; t < KPT; ++t) kvw[t] = kvn[t];
   }
 
   zero_orphans(bp, R);
@@ -510,7 +557,8 @@ bwd_long_kernel(const BwdParams bp) {
     for (int t = 0; t < KPT; ++t)
 #pragma unroll
       for (int c = 0; c < VC; c += 2)
-        *reinterpret_cast<float2*>(part + t * ld + c) = make_float2(dacc[t][c], dacc[t][c + 1]);
+        *reinterpret_cast<float2*>(part + t * ld + c) =
+            make_float2(dacc_t[t * TC + c], dacc_t[t * TC + c + 1]);
   }
 }
 
@@ -585,11 +633,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const int tiles = (ncv + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kCv;
   auto kern = bwd_small_kernel<R, COFF, D>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
-    return true;
-  }();
-  (void)attr;
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(kern, tx * ty, smem);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   const int64_t row_blocks = (p.C + ty - 1) / ty;
@@ -610,14 +654,16 @@ cudaError_t plan_small(const Problem& p, BwdShape* s) {
   return plan_small_d<R, COFF, 0>(p, s);
 }
 
-template <int R, int COFF>
-cudaError_t plan_long(const Problem& p, BwdShape* s) {
+template <int R, int COFF, int D>
+cudaError_t plan_long_d(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
   constexpr int NT = LongShape<W>::kThreads;
   const int ncv = p.d / LongShape<W>::kVc;
   const int tiles = (ncv + 31) / 32;
-  auto kern = bwd_long_kernel<R, COFF>;
-  const int occ = occupancy(kern, NT, 0);
+  auto kern = bwd_long_kernel<R, COFF, D>;
+  constexpr size_t smem = sizeof(float) * W * 32 * LongShape<W>::kVc;  // dape sums of the tile
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem)) return e;
+  const int occ = occupancy(kern, NT, smem);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy > p.C) gy = p.C;
   if (gy < 1) gy = 1;
@@ -629,9 +675,16 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
   if (gy > 65535) gy = 65535;
   s->grid = dim3(tiles, (unsigned)gy);
   s->block = dim3(32, LongShape<W>::kNch);
-  s->smem = 0;
+  s->smem = smem;
   s->groups = (int32_t)gy;
   return cudaSuccess;
+}
+
+template <int R, int COFF>
+cudaError_t plan_long(const Problem& p, BwdShape* s) {
+  if (p.d == 512) return plan_long_d<R, COFF, 512>(p, s);
+  if (p.d == 128) return plan_long_d<R, COFF, 128>(p, s);
+  return plan_long_d<R, COFF, 0>(p, s);
 }
 
 template <int R, int COFF>
@@ -647,7 +700,12 @@ cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream
 
 template <int R, int COFF>
 cudaError_t run_long(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  bwd_long_kernel<R, COFF><<<s.grid, s.block, s.smem, stream>>>(b);
+  if (b.p.d == 512)
+    bwd_long_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
+  else if (b.p.d == 128)
+    bwd_long_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
+  else
+    bwd_long_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
   return cudaGetLastError();
 }
 

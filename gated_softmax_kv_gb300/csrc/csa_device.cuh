@@ -74,9 +74,9 @@ __device__ __forceinline__ float softmax_exp(float x) {
 
 // exp(x) as 2^(x log2 e) with a single rounding of the product (no error
 // term): relative error about |x| 2^-24 from the product plus that of
-// ex2.approx. Clamp and NaN handling as softmax_exp.
+// ex2.approx. No clamp: ex2.approx.ftz gives +0 for -inf and flushes every
+// result below 2^-126 (all x < -87.4) to +0, and NaN stays NaN.
 __device__ __forceinline__ float softmax_exp_fast(float x) {
-  x = max_nan(x, -100.0f);
   return ex2_approx_ftz(__fmul_rn(x, __int_as_float(0x3fb8aa3b)));
 }
 

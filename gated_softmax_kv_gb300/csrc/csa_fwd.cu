@@ -28,6 +28,8 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "csa_device.cuh"
 #include "csa_internal.h"
@@ -160,7 +162,7 @@ fwd_small_kernel(const FwdParams f) {
 constexpr int kLongRows = 8;  // warps per CTA
 constexpr int kBatch = 8;     // window slots per batch
 
-template <int R, int COFF>
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(32 * kLongRows, 2)
 fwd_long_kernel(const FwdParams f, const int split) {
   constexpr int W = COFF * R;
@@ -170,7 +172,7 @@ fwd_long_kernel(const FwdParams f, const int split) {
   // [parity][warp][m, den, acc x 4 columns][lane]
   __shared__ float part[2][kLongRows][12][32];
   const Problem& p = f.p;
-  const int d = p.d;
+  const int d = D > 0 ? D : p.d;  // D > 0: slot offsets become immediates
   const int ncv = d / 4;
   const int cv = blockIdx.x * 32 + threadIdx.x;
   const bool col_ok = cv < ncv;
@@ -328,11 +330,7 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   const int tiles = (nvec + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kVec;
   auto kern = fwd_small_kernel<R, COFF, D>;
-  static bool attr = [&] {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
-    return true;
-  }();
-  (void)attr;
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(kern, tx * ty, smem);
   const int64_t row_blocks = (f.p.C + ty - 1) / ty;
   int64_t gy = (int64_t)sm_count() * occ / tiles;
@@ -371,7 +369,8 @@ cudaError_t launch_long(const FwdParams& f, cudaStream_t stream) {
          f.p.C * tiles * split < (int64_t)CSA_FWD_SPLIT_WARPS)
     split *= 2;
 #endif
-  auto kern = fwd_long_kernel<R, COFF>;
+  auto kern = f.p.d == 512 ? fwd_long_kernel<R, COFF, 512>
+             : f.p.d == 128 ? fwd_long_kernel<R, COFF, 128> : fwd_long_kernel<R, COFF, 0>;
   const int rows_per_cta = kLongRows / split;
   const int occ = occupancy(kern, 32 * kLongRows, 0);
   const int64_t row_blocks = (f.p.C + rows_per_cta - 1) / rows_per_cta;
@@ -416,6 +415,19 @@ cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
     case 128 * 4 + 2: return launch_long<128, 2>(f, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  if (cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))
+    return e;
+  done.insert({kernel, dev});
+  return cudaSuccess;
 }
 
 int sm_count() {

@@ -56,6 +56,9 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); the attribute is per device.
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
 
 }  // namespace csa
 
