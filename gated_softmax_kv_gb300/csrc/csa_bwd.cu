@@ -12,18 +12,21 @@
 // Padding rows (b >= cu_seqlens_comp[-1]) are not visited at all.
 //
 // dape is reduced deterministically in two levels, without atomics: each CTA
-// accumulates its rows' logit gradients in registers (rows in a fixed order),
-// combines its threads in a fixed order and writes one fp32 partial per row
-// group; dape_reduce then sums the partials in a fixed order and overwrites dape.
+// accumulates its rows' logit gradients (rows in a fixed order; registers in
+// bwd_small, a shared-memory table in bwd_long), combines its threads in a
+// fixed order and writes one fp32 partial per row group; dape_reduce then
+// sums the partials in a fixed order and overwrites dape.
 //
 // Kernel shapes mirror the forward (csa_fwd.cu): bwd_small keeps a W <= 8
-// window of 4 columns per thread in registers and follows the plain eager
-// operation order (p = e / den per slot, sequential sums); bwd_chunk splits W >= 16 windows over threadIdx.y chunks of
-// 8 slots and merges the per-chunk (max, sum exp) and S partials in a fixed
-// order through shared memory.
+// window of 4 columns per thread in registers and follows the eager
+// operation order (m, e, den, p = e * (1 / den), sequential sums); bwd_long
+// splits W >= 16 windows over warps of 8 or 16 slots, merges the per-chunk
+// (max, sum exp, sum (g kv) exp) triples in a fixed order through shared
+// memory and prefetches the next row while it computes the current one.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "csa_bwd_common.cuh"
 #include "csa_device.cuh"
 #include "csa_internal.h"
 
@@ -33,49 +36,20 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// exp of the long-window backward's per-element weights. Windows of 16 slots
-// and more have no bitwise target (the page aims at bit identity for ratios 2
-// and 4 only), so they take the single-rounding softmax_exp_fast.
-#ifndef CSA_BWD_LONG_EXP
-#define CSA_BWD_LONG_EXP softmax_exp_fast
+// exp and division of the small-window backward's per-element weights. The
+// default is the single-rounding exp and p = e * RN(1 / den): 5% faster at
+// the headline than the compensated exp with the correctly rounded e / den
+// (CSA_BWD_SMALL_EXP=softmax_exp, CSA_BWD_SMALL_DIV_RN=1), for 0.0012%
+// instead of 0.0008% of dkv and 0.0045% instead of 0.0040% of dscore
+// differing from the oracle by one bf16 step; neither reaches bit identity.
+#ifndef CSA_BWD_SMALL_EXP
+#define CSA_BWD_SMALL_EXP softmax_exp_fast
 #endif
-// Long-window backward: windows of at least this many slots give each warp 16
-// slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
-#ifndef CSA_BWD_LONG_KPT16_FROM
-#define CSA_BWD_LONG_KPT16_FROM 256
+#ifndef CSA_BWD_SMALL_DIV_RN
+#define CSA_BWD_SMALL_DIV_RN 0
 #endif
-constexpr int kCv = 4;    // columns per thread in the chunked kernel (8-byte vectors)
+constexpr int kCv = 4;  // columns per thread (8-byte vectors)
 
-
-// Zeros for the positions no row reads that belong to nobody's window:
-// segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
-// Spread over every CTA of the launch.
-__device__ __forceinline__ void zero_orphans(const BwdParams& bp, int ratio) {
-  const Problem& p = bp.p;
-  const int64_t ld = (int64_t)p.coff * p.d;
-  const int64_t vpt = ld / kVec;  // 16-byte vectors per token row
-  const int nthr = blockDim.x * blockDim.y;
-  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-  const int64_t fb = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
-  const int64_t nb = (int64_t)gridDim.x * gridDim.y;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  for (int64_t s = fb; s < p.nseq; s += nb) {
-    int64_t lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
-    if (hi - lo >= ratio || hi <= lo) continue;
-    lo = lo < 0 ? 0 : lo;
-    hi = hi > p.T ? p.T : hi;
-    for (int64_t v = lo * vpt + tid; v < hi * vpt; v += nthr) {
-      st_stream(bp.dkv + v * kVec, zero);
-      st_stream(bp.dscore + v * kVec, zero);
-    }
-  }
-  int64_t end = __ldg(p.cu + p.nseq);
-  end = end < 0 ? 0 : (end > p.T ? p.T : end);
-  for (int64_t v = end * vpt + fb * nthr + tid; v < p.T * vpt; v += nb * nthr) {
-    st_stream(bp.dkv + v * kVec, zero);
-    st_stream(bp.dscore + v * kVec, zero);
-  }
-}
 
 // Small window (W <= 8): blockDim = (TX, TY); a thread owns 4 consecutive
 // columns (8-byte vectors) of one row at a time, rows strided by the grid.
@@ -142,7 +116,7 @@ bwd_small_kernel(const BwdParams bp) {
       }
       const uint2 gv = ld_stream8(bp.grad_out + b * d + j0);
 
-      // z = score + ape, then in place e = exp(z - m), then p = e / den
+      // z = score + ape, then in place e = exp(z - m), then p = e * (1 / den)
       float pz[W][kCv];
 #pragma unroll
       for (int k = 0; k < W; ++k) {
@@ -165,12 +139,17 @@ bwd_small_kernel(const BwdParams bp) {
           float den = 0.0f;
 #pragma unroll
           for (int k = 0; k < W; ++k) {
-            pz[k][c] = softmax_exp(__fsub_rn(pz[k][c], m));
+            pz[k][c] = CSA_BWD_SMALL_EXP(__fsub_rn(pz[k][c], m));
             den = __fadd_rn(den, pz[k][c]);
           }
           const float y = __frcp_rn(den);
+#if CSA_BWD_SMALL_DIV_RN
 #pragma unroll
           for (int k = 0; k < W; ++k) pz[k][c] = div_rn_by_rcp(pz[k][c], den, y);
+#else
+#pragma unroll
+          for (int k = 0; k < W; ++k) pz[k][c] = __fmul_rn(pz[k][c], y);
+#endif
           g[h] = bf16_at(c2 ? gv.y : gv.x, h);
           float acc = 0.0f;
 #pragma unroll
@@ -264,304 +243,6 @@ bwd_small_kernel(const BwdParams bp) {
   }
 }
 
-// Long window (W >= 16): blockDim = (32, NCH) with NCH = W / KPT (KPT = 8
-// slots per warp, 16 for W = 256). Warp y owns window slots
-// [KPT y, KPT y + KPT) and lane l owns VC consecutive columns of a
-// (32 VC)-column tile (blockIdx.x), so every load and store of a warp covers
-// 32 VC * 2 contiguous bytes of one token row. The CTA walks rows
-// b = blockIdx.y, blockIdx.y + gridDim.y, ... and per row:
-//   phase 1  z = score + ape, the chunk's max m_c, e = exp(z - m_c), sum e and
-//            T_c = sum (g kv) e
-//   merge    (max, sum, T) of the NCH chunks of a column, in a fixed order:
-//            NCH/VC threads take VC chunks each, then a butterfly over those
-//            lanes (commutative combines, so every lane gets the same bits);
-//            S = sum (g kv) p = T / den
-//   phase 2  p = e * (exp(m_c - M) / den) (one exp and one reciprocal per
-//            column and chunk), dscore = p (g kv - S), dkv = g p, stores; dape
-//            accumulates in shared memory (each thread owns KPT slots x VC
-//            columns of the [W][TC] table, so no barrier guards it)
-// Two barriers per row. The next row's kv, score and grad_out loads are
-// issued before the merge, so they are in flight through the merge and
-// phase 2 (one CTA of NCH warps per SM would otherwise leave HBM idle while
-// it computes).
-template <int W>
-struct LongShape {
-  static constexpr int kKpt = W >= CSA_BWD_LONG_KPT16_FROM ? 16 : 8;                   // slots per warp
-  static constexpr int kVc = (W >= CSA_BWD_LONG_KPT16_FROM || W <= 16) ? 2 : 4;        // columns per lane
-  static constexpr int kNch = W / kKpt;                      // warps per CTA
-  static constexpr int kThreads = 32 * kNch;
-  static constexpr int kMinBlocks = kThreads >= 512 ? 1 : 512 / kThreads;  // <= 128 registers
-  static_assert(kNch % kVc == 0, "each column's chunks split evenly over its merge threads");
-};
-
-template <int VC>
-struct ColVec;
-template <>
-struct ColVec<2> {
-  using T = uint32_t;
-  static __device__ __forceinline__ T load(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint32_t*>(p)); }
-  static __device__ __forceinline__ void store(uint16_t* p, T v) { __stcs(reinterpret_cast<uint32_t*>(p), v); }
-  static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(v, c); }
-  static __device__ __forceinline__ T zero() { return 0u; }
-  static __device__ __forceinline__ T ninf() { return kNegInfBf16x2; }
-  static __device__ __forceinline__ T pack(const float* x) { return pack_bf16x2(x[0], x[1]); }
-};
-template <>
-struct ColVec<4> {
-  using T = uint2;
-  static __device__ __forceinline__ T load(const uint16_t* p) { return ld_stream8(p); }
-  static __device__ __forceinline__ void store(uint16_t* p, T v) { st_stream8(p, v); }
-  static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(c < 2 ? v.x : v.y, c & 1); }
-  static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
-  static __device__ __forceinline__ T ninf() { return make_uint2(kNegInfBf16x2, kNegInfBf16x2); }
-  static __device__ __forceinline__ T pack(const float* x) {
-    return make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-  }
-};
-
-// fixed-order merge of (max, sum exp, sum (g kv) exp) triples rescaled to the
-// common max: m = max, s = s_a e^(m_a - m) + s_b e^(m_b - m), t likewise.
-// Symmetric in a and b, so both lanes of a butterfly step get the same bits.
-__device__ __forceinline__ void merge_max_sum2(float& m, float& s, float& t, float mb, float sb,
-                                               float tb) {
-  const float kNegInf = __int_as_float(0xff800000);
-  const float mn = max_nan(m, mb);
-  const float mu = mn == kNegInf ? 0.0f : mn;
-  const float fa = softmax_exp(__fsub_rn(m, mu)), fb = softmax_exp(__fsub_rn(mb, mu));
-  s = __fadd_rn(__fmul_rn(s, fa), __fmul_rn(sb, fb));
-  t = __fadd_rn(__fmul_rn(t, fa), __fmul_rn(tb, fb));
-  m = mn;
-}
-
-// D > 0 fixes head_dim at compile time (slot offsets become immediates);
-// D == 0 reads it from the problem.
-template <int R, int COFF, int D>
-__global__ void __launch_bounds__(LongShape<COFF * R>::kThreads, LongShape<COFF * R>::kMinBlocks)
-bwd_long_kernel(const BwdParams bp) {
-  constexpr int W = COFF * R;
-  constexpr int KPT = LongShape<W>::kKpt;
-  constexpr int VC = LongShape<W>::kVc;
-  constexpr int NCH = LongShape<W>::kNch;
-  constexpr int NT = LongShape<W>::kThreads;
-  constexpr int TC = 32 * VC;      // tile columns
-  constexpr int G = NCH / VC;      // merge threads per column
-  constexpr int LDS = TC + 1;      // padded row stride of the chunk tables
-  using S = Slot<R, COFF>;
-  using V = ColVec<VC>;
-  const Problem& p = bp.p;
-  const int d = D > 0 ? D : p.d;
-  const int lane = threadIdx.x, y = threadIdx.y;
-  const int tid = y * 32 + lane;
-  const int ncv = d / VC;
-  const int cv = blockIdx.x * 32 + lane;
-  const bool col_ok = cv < ncv;
-  const int64_t ld = (int64_t)COFF * d;
-  const int j0 = cv * VC;
-  const int k0 = y * KPT;
-  const float kNegInf = __int_as_float(0xff800000);
-
-  __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
-  __shared__ float M_s[TC], D_s[TC], S_s[TC];
-  // dape sums of the tile, [W][TC]; each cell belongs to one thread
-  extern __shared__ float dacc_s[];
-  float* dacc_t = dacc_s + k0 * TC + lane * VC;
-#pragma unroll
-  for (int t = 0; t < KPT; ++t)
-#pragma unroll
-    for (int c = 0; c < VC; ++c) dacc_t[t * TC + c] = 0.0f;
-
-  // this thread's APE values (slots k0.., columns j0..) are re-read per row through L1
-  const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
-
-  // merge thread layout: column mc of the tile, group member mq (G per column)
-  const int mc = tid / G, mq = tid % G;
-
-  // The next row's kv, score and grad_out are loaded while the current row
-  // merges and runs phase 2 (score into the registers phase 1 has consumed).
-  typename V::T kvw[KPT], scw[KPT], gw = V::zero();
-  auto offset = [&](const RowInfo& r) {
-    return r.base * ld + S::tok(0, k0) * ld + S::half(k0) * d + j0;
-  };
-  auto loads = [&](int64_t rb, const RowInfo& r, typename V::T (&kvb)[KPT], typename V::T& gb) {
-    // rows past capacity and rows that break the preconditions load nothing
-    if (rb >= p.C || !row_in_bounds<R, COFF>(r, p.T)) {
-#pragma unroll
-      for (int t = 0; t < KPT; ++t) kvb[t] = V::zero();
-      return;
-    }
-    const bool act = col_ok && !S::masked(r.first, k0);
-    const int64_t off = offset(r);
-#pragma unroll
-    for (int t = 0; t < KPT; ++t) {
-      kvb[t] = act ? V::load(p.kv + off + t * ld) : V::zero();
-      scw[t] = act ? V::load(p.score + off + t * ld) : V::ninf();
-    }
-    gb = col_ok ? V::load(bp.grad_out + rb * d + j0) : V::zero();
-  };
-
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  int64_t b = blockIdx.y;
-  RowInfo ri{};
-  if (b < true_rows) {
-    ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
-    loads(b, ri, kvw, gw);
-  }
-  for (; b < true_rows;) {
-    const bool row_ok = row_in_bounds<R, COFF>(ri, p.T);  // uniform over the CTA
-    const bool active = col_ok && !S::masked(ri.first, k0);
-    const int64_t off = offset(ri);
-    const bool compute = row_ok && b < p.C;  // uniform over the CTA
-    float g[VC], mloc[VC];
-    float pz[KPT][VC];
-    if (compute) {
-#pragma unroll
-      for (int c = 0; c < VC; ++c) g[c] = V::elem(gw, c);
-#pragma unroll
-      for (int t = 0; t < KPT; ++t) {
-#pragma unroll
-        for (int c = 0; c < VC; c += 2) {
-          const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld + c))
-                                  : make_float2(0.0f, 0.0f);
-          pz[t][c] = __fadd_rn(V::elem(scw[t], c), a.x);
-          pz[t][c + 1] = __fadd_rn(V::elem(scw[t], c + 1), a.y);
-        }
-      }
-      // phase 1: per column, the chunk's max m_c, e = exp(z - m_c), its sum
-      // and T_c = sum (g kv) e; one fixed-order merge of (max, sum, T) then
-      // gives the row's max M, den and S = T / den together
-#pragma unroll
-      for (int c = 0; c < VC; ++c) {
-        float m = pz[0][c];
-#pragma unroll
-        for (int t = 1; t < KPT; ++t) m = max_nan(m, pz[t][c]);
-        const float mu = m == kNegInf ? 0.0f : m;  // an all -inf chunk contributes 0
-        float sum = 0.0f, tsum = 0.0f;
-#pragma unroll
-        for (int t = 0; t < KPT; ++t) {
-          pz[t][c] = CSA_BWD_LONG_EXP(__fsub_rn(pz[t][c], mu));
-          sum = __fadd_rn(sum, pz[t][c]);
-          tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c]));
-        }
-        mloc[c] = m;
-        m_s[y * LDS + lane * VC + c] = m;
-        d_s[y * LDS + lane * VC + c] = sum;
-        s_s[y * LDS + lane * VC + c] = tsum;
-      }
-    }
-    // prefetch the next row of this CTA
-    const int64_t bn = b + gridDim.y;
-    RowInfo rn{};
-    typename V::T kvn[KPT], gn = V::zero();
-    if (bn < true_rows) {
-      rn = row_info(p.cu, p.cuc, p.nseq, bn, true_rows, R);
-      loads(bn, rn, kvn, gn);
-    }
-    if (compute) {
-      __syncthreads();
-      {
-        float m = m_s[(mq * VC) * LDS + mc], sm = d_s[(mq * VC) * LDS + mc];
-        float tm = s_s[(mq * VC) * LDS + mc];
-#pragma unroll
-        for (int i = 1; i < VC; ++i)
-          merge_max_sum2(m, sm, tm, m_s[(mq * VC + i) * LDS + mc], d_s[(mq * VC + i) * LDS + mc],
-                         s_s[(mq * VC + i) * LDS + mc]);
-#pragma unroll
-        for (int mask = 1; mask < G; mask <<= 1)
-          merge_max_sum2(m, sm, tm, __shfl_xor_sync(0xffffffffu, m, mask),
-                         __shfl_xor_sync(0xffffffffu, sm, mask), __shfl_xor_sync(0xffffffffu, tm, mask));
-        if (mq == 0) {
-          M_s[mc] = m;
-          D_s[mc] = sm;
-          S_s[mc] = __fdiv_rn(tm, sm);
-        }
-      }
-      __syncthreads();
-      // phase 2: p = e exp(m_c - M) / den, dscore = p (g kv - S), dkv = g p
-#pragma unroll
-      for (int c = 0; c < VC; ++c) {
-        const float M = M_s[lane * VC + c];
-        const float den = D_s[lane * VC + c];
-        const float mu = M == kNegInf ? 0.0f : M;
-        const float ml = mloc[c] == kNegInf ? 0.0f : mloc[c];
-        const float f = softmax_exp(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
-        // one scale per column and chunk: f / den (no per-element division;
-        // like the exp above, not correctly rounded)
-        const float fy = __fmul_rn(f, __frcp_rn(den));
-#pragma unroll
-        for (int t = 0; t < KPT; ++t) pz[t][c] = __fmul_rn(pz[t][c], fy);
-      }
-      float Sv[VC];
-#pragma unroll
-      for (int c = 0; c < VC; ++c) Sv[c] = S_s[lane * VC + c];
-#pragma unroll
-      for (int t = 0; t < KPT; ++t) {
-        float dz[VC], dk[VC];
-#pragma unroll
-        for (int c = 0; c < VC; ++c) {
-          dz[c] = __fmul_rn(pz[t][c], __fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]));
-          dk[c] = __fmul_rn(g[c], pz[t][c]);
-          dacc_t[t * TC + c] = __fadd_rn(dacc_t[t * TC + c], dz[c]);
-        }
-        if (active) {
-          V::store(bp.dkv + off + t * ld, V::pack(dk));
-          V::store(bp.dscore + off + t * ld, V::pack(dz));
-        }
-      }
-    } else if (row_ok && active) {
-      // a row past capacity has no output slot: zero gradient at its positions
-#pragma unroll
-      for (int t = 0; t < KPT; ++t) {
-        V::store(bp.dkv + off + t * ld, V::zero());
-        V::store(bp.dscore + off + t * ld, V::zero());
-      }
-    }
-    if (row_ok && ri.last) {
-      // unread positions owned by the segment's last row, for this column tile:
-      // its block's first-half columns (coff 2) and the segment tail
-      const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
-      const int64_t n_first = COFF == 2 ? (int64_t)R * 32 : 0;
-      const int64_t n_tail = (tail_end - (ri.base + R)) * COFF * 32;
-      for (int64_t i = tid; i < n_first + n_tail; i += NT) {
-        int64_t tok;
-        int h, x;
-        if (i < n_first) {
-          tok = ri.base + i / 32;
-          h = 0;
-          x = (int)(i % 32);
-        } else {
-          const int64_t q = i - n_first;
-          tok = ri.base + R + q / (COFF * 32);
-          h = (int)((q / 32) % COFF);
-          x = (int)(q % 32);
-        }
-        const int col_v = blockIdx.x * 32 + x;
-        if (col_v >= ncv) continue;
-        V::store(bp.dkv + tok * ld + h * d + col_v * VC, V::zero());
-        V::store(bp.dscore + tok * ld + h * d + col_v * VC, V::zero());
-      }
-    }
-    b = bn;
-    ri = rn;
-    gw = gn;
-#pragma unroll
-    for (int t = 0; t < KPT; ++t) kvw[t] = kvn[t];
-  }
-
-  zero_orphans(bp, R);
-
-  // each (slot, column) of the tile belongs to exactly one thread
-  if (col_ok) {
-    float* part = bp.partial + (int64_t)blockIdx.y * (R * ld) + (int64_t)S::ape_row(k0) * ld +
-                  S::half(k0) * d + j0;
-#pragma unroll
-    for (int t = 0; t < KPT; ++t)
-#pragma unroll
-      for (int c = 0; c < VC; c += 2)
-        *reinterpret_cast<float2*>(part + t * ld + c) =
-            make_float2(dacc_t[t * TC + c], dacc_t[t * TC + c + 1]);
-  }
-}
-
 // dape[e] = sum over groups g of partial[g][e] in two fixed levels. A lane
 // owns 4 consecutive elements (16-byte loads; every group row starts on a
 // 32-byte boundary because ratio * coff * d is a multiple of 8). Lane y of the
@@ -615,15 +296,6 @@ dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n
   }
 }
 
-template <typename K>
-int occupancy(K kernel, int threads, size_t smem) {
-  int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess ||
-      blocks < 1)
-    blocks = 1;
-  return blocks;
-}
-
 template <int R, int COFF, int D>
 cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
@@ -634,7 +306,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const size_t smem = sizeof(float) * W * tx * kCv;
   auto kern = bwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
-  const int occ = occupancy(kern, tx * ty, smem);
+  const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   const int64_t row_blocks = (p.C + ty - 1) / ty;
   if (gy > row_blocks) gy = row_blocks;
@@ -654,39 +326,6 @@ cudaError_t plan_small(const Problem& p, BwdShape* s) {
   return plan_small_d<R, COFF, 0>(p, s);
 }
 
-template <int R, int COFF, int D>
-cudaError_t plan_long_d(const Problem& p, BwdShape* s) {
-  constexpr int W = COFF * R;
-  constexpr int NT = LongShape<W>::kThreads;
-  const int ncv = p.d / LongShape<W>::kVc;
-  const int tiles = (ncv + 31) / 32;
-  auto kern = bwd_long_kernel<R, COFF, D>;
-  constexpr size_t smem = sizeof(float) * W * 32 * LongShape<W>::kVc;  // dape sums of the tile
-  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem)) return e;
-  const int occ = occupancy(kern, NT, smem);
-  int64_t gy = (int64_t)sm_count() * occ / tiles;
-  if (gy > p.C) gy = p.C;
-  if (gy < 1) gy = 1;
-  // even out the rows per CTA
-  if (p.C > 0) {
-    const int64_t passes = (p.C + gy - 1) / gy;
-    gy = (p.C + passes - 1) / passes;
-  }
-  if (gy > 65535) gy = 65535;
-  s->grid = dim3(tiles, (unsigned)gy);
-  s->block = dim3(32, LongShape<W>::kNch);
-  s->smem = smem;
-  s->groups = (int32_t)gy;
-  return cudaSuccess;
-}
-
-template <int R, int COFF>
-cudaError_t plan_long(const Problem& p, BwdShape* s) {
-  if (p.d == 512) return plan_long_d<R, COFF, 512>(p, s);
-  if (p.d == 128) return plan_long_d<R, COFF, 128>(p, s);
-  return plan_long_d<R, COFF, 0>(p, s);
-}
-
 template <int R, int COFF>
 cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
   if (b.p.d == 512)
@@ -698,45 +337,27 @@ cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream
   return cudaGetLastError();
 }
 
-template <int R, int COFF>
-cudaError_t run_long(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  if (b.p.d == 512)
-    bwd_long_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
-  else if (b.p.d == 128)
-    bwd_long_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
-  else
-    bwd_long_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
-  return cudaGetLastError();
-}
-
-#define CSA_BWD_DISPATCH(FN_SMALL, FN_LONG, ...)                 \
+#define CSA_BWD_SMALL_DISPATCH(FN, ...)                       \
   switch (p.ratio * 4 + p.coff) {                                 \
-    case 2 * 4 + 1: return FN_SMALL<2, 1>(__VA_ARGS__);           \
-    case 2 * 4 + 2: return FN_SMALL<2, 2>(__VA_ARGS__);           \
-    case 4 * 4 + 1: return FN_SMALL<4, 1>(__VA_ARGS__);           \
-    case 4 * 4 + 2: return FN_SMALL<4, 2>(__VA_ARGS__);           \
-    case 8 * 4 + 1: return FN_SMALL<8, 1>(__VA_ARGS__);           \
-    case 8 * 4 + 2: return FN_LONG<8, 2>(__VA_ARGS__);           \
-    case 16 * 4 + 1: return FN_LONG<16, 1>(__VA_ARGS__);         \
-    case 16 * 4 + 2: return FN_LONG<16, 2>(__VA_ARGS__);         \
-    case 32 * 4 + 1: return FN_LONG<32, 1>(__VA_ARGS__);         \
-    case 32 * 4 + 2: return FN_LONG<32, 2>(__VA_ARGS__);         \
-    case 64 * 4 + 1: return FN_LONG<64, 1>(__VA_ARGS__);         \
-    case 64 * 4 + 2: return FN_LONG<64, 2>(__VA_ARGS__);         \
-    case 128 * 4 + 1: return FN_LONG<128, 1>(__VA_ARGS__);       \
-    case 128 * 4 + 2: return FN_LONG<128, 2>(__VA_ARGS__);       \
-    default: return cudaErrorInvalidValue;                        \
+    case 2 * 4 + 1: return FN<2, 1>(__VA_ARGS__);                 \
+    case 2 * 4 + 2: return FN<2, 2>(__VA_ARGS__);                 \
+    case 4 * 4 + 1: return FN<4, 1>(__VA_ARGS__);                 \
+    case 4 * 4 + 2: return FN<4, 2>(__VA_ARGS__);                 \
+    case 8 * 4 + 1: return FN<8, 1>(__VA_ARGS__);                 \
+    default: break;                                               \
   }
 
 }  // namespace
 
 cudaError_t plan_bwd(const Problem& p, BwdShape* shape) {
-  CSA_BWD_DISPATCH(plan_small, plan_long, p, shape)
+  CSA_BWD_SMALL_DISPATCH(plan_small, p, shape)
+  return plan_bwd_long(p, shape);  // windows of 16 slots and more
 }
 
 cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
   const Problem& p = b.p;
-  CSA_BWD_DISPATCH(run_small, run_long, b, shape, stream)
+  CSA_BWD_SMALL_DISPATCH(run_small, b, shape, stream)
+  return launch_bwd_long(b, shape, stream);
 }
 
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,

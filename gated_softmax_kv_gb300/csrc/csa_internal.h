@@ -51,11 +51,17 @@ cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream);
 
 cudaError_t plan_bwd(const Problem& p, BwdShape* shape);
 cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
+// Windows of 16 slots and more (csa_fwd_long.cu, csa_bwd_long.cu).
+cudaError_t launch_fwd_long(const FwdParams& f, cudaStream_t stream);
+cudaError_t plan_bwd_long(const Problem& p, BwdShape* shape);
+cudaError_t launch_bwd_long(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
                                cudaStream_t stream);
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// Resident CTAs per SM of a kernel (at least 1).
+int occupancy(const void* kernel, int threads, size_t smem);
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device); the attribute is per device.
 cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
