@@ -58,6 +58,8 @@ constexpr int kCv = 4;  // columns per thread (8-byte vectors)
 template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_small_kernel(const BwdParams bp) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = bp.p;
@@ -255,6 +257,8 @@ constexpr int kReduceMaxLanes = 32;
 __global__ void __launch_bounds__(32 * kReduceMaxLanes)
 dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n4,
                    float4* __restrict__ dape) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   __shared__ float4 red[kReduceMaxLanes][32];
   const int Y = blockDim.y;
   const int64_t e = (int64_t)blockIdx.x * 32 + threadIdx.x;
@@ -328,13 +332,9 @@ cudaError_t plan_small(const Problem& p, BwdShape* s) {
 
 template <int R, int COFF>
 cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  if (b.p.d == 512)
-    bwd_small_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
-  else if (b.p.d == 128)
-    bwd_small_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
-  else
-    bwd_small_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
-  return cudaGetLastError();
+  auto kern = b.p.d == 512 ? bwd_small_kernel<R, COFF, 512>
+             : b.p.d == 128 ? bwd_small_kernel<R, COFF, 128> : bwd_small_kernel<R, COFF, 0>;
+  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
 }
 
 #define CSA_BWD_SMALL_DISPATCH(FN, ...)                       \
@@ -372,9 +372,9 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
   int lanes = 1;
   while (lanes < kReduceMaxLanes && lanes * 2 <= groups && blocks * 32 * lanes * 2 <= 2 * 152 * 2048)
     lanes *= 2;
-  dape_reduce_kernel<<<(unsigned)blocks, dim3(32, lanes), 0, stream>>>(
-      reinterpret_cast<const float4*>(partial), groups, n4, reinterpret_cast<float4*>(dape));
-  return cudaGetLastError();
+  return launch_dependent(dape_reduce_kernel, dim3((unsigned)blocks), dim3(32, lanes), 0, stream,
+                          reinterpret_cast<const float4*>(partial), groups, n4,
+                          reinterpret_cast<float4*>(dape));
 }
 
 }  // namespace csa

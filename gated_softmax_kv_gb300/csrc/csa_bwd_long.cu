@@ -99,6 +99,8 @@ __device__ __forceinline__ void merge_max_sum2(float& m, float& s, float& t, flo
 template <int R, int COFF, int D>
 __global__ void __launch_bounds__(LongShape<COFF * R>::kThreads, LongShape<COFF * R>::kMinBlocks)
 bwd_long_kernel(const BwdParams bp) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   constexpr int W = COFF * R;
   constexpr int KPT = LongShape<W>::kKpt;
   constexpr int VC = LongShape<W>::kVc;
@@ -358,13 +360,9 @@ cudaError_t plan_long(const Problem& p, BwdShape* s) {
 
 template <int R, int COFF>
 cudaError_t run_long(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  if (b.p.d == 512)
-    bwd_long_kernel<R, COFF, 512><<<s.grid, s.block, s.smem, stream>>>(b);
-  else if (b.p.d == 128)
-    bwd_long_kernel<R, COFF, 128><<<s.grid, s.block, s.smem, stream>>>(b);
-  else
-    bwd_long_kernel<R, COFF, 0><<<s.grid, s.block, s.smem, stream>>>(b);
-  return cudaGetLastError();
+  auto kern = b.p.d == 512 ? bwd_long_kernel<R, COFF, 512>
+             : b.p.d == 128 ? bwd_long_kernel<R, COFF, 128> : bwd_long_kernel<R, COFF, 0>;
+  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
 }
 
 #define CSA_BWD_LONG_DISPATCH(FN, ...)                        \

@@ -101,6 +101,23 @@ __device__ __forceinline__ float div_rn_by_rcp(float a, float b, float y) {
   return __fmaf_rn(r, y, q);
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+
+// Every kernel of the library is launched with programmatic stream
+// serialization (launch_dependent below): it may become resident while the
+// previous kernel on the stream drains, and grid_dependency_wait holds it
+// until that grid has completed and its memory operations are visible. So
+// each kernel calls it before its first global access (read or write), and
+// allow_dependent_launch right after, letting the next kernel's launch
+// overlap this one's tail (it can only start once every CTA of this grid
+// has started). Both are no-ops under a normal launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- memory ----------------------------------------------------------------
 
 // kv / score / grad_out are read exactly once: streaming (evict-first) loads.

@@ -57,6 +57,8 @@ constexpr int kThreads = 256;
 template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_small_kernel(const FwdParams f) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   constexpr int W = COFF * R;
   using S = Slot<R, COFF>;
   const Problem& p = f.p;
@@ -164,8 +166,7 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   if (gy < 1) gy = 1;
   if (gy > row_blocks) gy = row_blocks;
   if (gy > 65535) gy = 65535;
-  kern<<<dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream>>>(f);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream, f);
 }
 
 template <int R, int COFF>

@@ -37,6 +37,8 @@ constexpr int kBatch = 8;     // window slots per batch
 template <int R, int COFF, int D>
 __global__ void __launch_bounds__(32 * kLongRows, 2)
 fwd_long_kernel(const FwdParams f, const int split) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   constexpr int W = COFF * R;
   constexpr int NB = W / kBatch;  // batches per window, >= 2
   using S = Slot<R, COFF>;
@@ -217,8 +219,7 @@ cudaError_t launch_long(const FwdParams& f, cudaStream_t stream) {
   const int64_t passes = (row_blocks + gy - 1) / gy;
   gy = (row_blocks + passes - 1) / passes;
   if (gy > 65535) gy = 65535;
-  kern<<<dim3(tiles, (unsigned)gy), dim3(32, kLongRows), 0, stream>>>(f, split);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(32, kLongRows), 0, stream, f, split);
 }
 
 }  // namespace

@@ -1,11 +1,37 @@
-// Internal interface between the C ABI (csa_api.cu) and the kernel
-// translation units (csa_fwd.cu, csa_bwd.cu). Not installed, not part of the ABI.
+// Internal interface between the C ABI (csa_api.cu, csa_noalloc.cu) and the
+// kernel translation units (csa_fwd.cu, csa_fwd_long.cu, csa_bwd.cu,
+// csa_bwd_long.cu). Not installed, not part of the ABI.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace csa {
+
+// Launches `kernel` on `stream` with programmatic stream serialization (the
+// kernel's launch may overlap the previous kernel's tail; the kernel waits for
+// that grid with griddepcontrol.wait before touching memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+#ifdef CSA_NO_PDL
+  cfg.numAttrs = 0;  // plain stream order (comparison builds)
+#else
+  cfg.numAttrs = 1;
+#endif
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // One Compressor call after host validation. Pointers are device pointers;
 // bf16 tensors travel as raw 16-bit patterns.
