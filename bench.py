@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="headline",
                     help="another seeded workload instead of the headline: r4d512, r2d128rag, "
                          "r128c1, or a pack `pack-r{ratio}c{coff}d{head_dim}-{n}x{len}`")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time one forward + backward step captured in a CUDA graph and replayed")
     ap.add_argument("--l2", choices=["auto", "flush", "warm"], default="auto",
                     help="flush L2 before every call (auto: when kv + score fit in twice the L2)")
     args = ap.parse_args()
@@ -401,6 +403,42 @@ def run_e2e(args, case, dev, stream, ranks):
     return el, h2d, d2h, KE
 
 
+def run_graph(args, fwd_g, bwd_g, l2, stream):
+    """One forward + backward step captured in a CUDA graph, replayed K times;
+    each replay timed with events on the replay stream (the L2 treatment of
+    the eager loop applies between replays)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fwd_g(int(side.cuda_stream))
+        bwd_g(int(side.cuda_stream))
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        h = int(torch.cuda.current_stream().cuda_stream)
+        fwd_g(h)
+        bwd_g(h)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for _ in range(args.warmup):
+        l2()
+        g.replay()
+    torch.cuda.synchronize()
+    for i in range(K):
+        l2()
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    return {"step_us": statistics.mean(ms) * 1e3, "step_us_median": statistics.median(ms) * 1e3,
+            "replays": K, "what": "fwd + bwd captured once in a CUDA graph, replay timed by events"}
+
+
 def run_gpu(args, rank, world, local):
     import numpy as np
     import torch
@@ -432,14 +470,20 @@ def run_gpu(args, rank, world, local):
     sh = int(stream.cuda_stream)
     nseq = case.num_seqs
 
-    def fwd():
+    def fwd_g(h):
         gsk.csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
-                                 cuc.data_ptr(), nseq, T, C, r, coff, d, out.data_ptr(), sh)
+                                 cuc.data_ptr(), nseq, T, C, r, coff, d, out.data_ptr(), h)
 
-    def bwd():
+    def bwd_g(h):
         gsk.csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
                                  cuc.data_ptr(), nseq, T, C, r, coff, d, grad_out.data_ptr(),
-                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh)
+                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), h)
+
+    def fwd():
+        fwd_g(sh)
+
+    def bwd():
+        bwd_g(sh)
 
     barrier = ranks.barrier
     # Small workloads would stay in the 129 MB L2 from one call to the next:
@@ -487,6 +531,8 @@ def run_gpu(args, rank, world, local):
     if flush:  # the scrubbing writes are not part of a step
         elapsed = (sum(fwd_ms) + sum(bwd_ms)) / 1e3
     elapsed = ranks.max(elapsed)
+
+    graph = run_graph(args, fwd_g, bwd_g, l2, stream) if args.graph else None
 
     # End to end through the same C ABI with host buffers. Every step copies its
     # inputs from pinned host memory to HBM, runs both calls and copies every
@@ -538,6 +584,7 @@ def run_gpu(args, rank, world, local):
         "e2e": {"value": T * KE * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": KE},
         "gpu_launches": 3 * K,
+        **({"graph": graph} if graph is not None else {}),
         "clocks": clk,
         "cpu_baseline": cpu,
     }
