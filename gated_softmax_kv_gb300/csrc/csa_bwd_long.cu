@@ -13,16 +13,22 @@ namespace csa {
 
 namespace {
 
-// exp of the long-window backward's per-element weights. Windows of 16 slots
-// and more have no bitwise target (the page aims at bit identity for ratios 2
-// and 4 only), so they take the single-rounding softmax_exp_fast.
+// exp of the long-window backward (per-element weights, chunk merges and the
+// rescaling of a chunk to the row max). Windows of 16 slots and more have no
+// bitwise target (the page aims at bit identity for ratios 2 and 4 only), so
+// they take the single-rounding softmax_exp_fast.
 #ifndef CSA_BWD_LONG_EXP
 #define CSA_BWD_LONG_EXP softmax_exp_fast
+#endif
+// T = sum (g kv) e accumulated with one FMA per slot (default) or a rounded
+// product and an add
+#ifndef CSA_BWD_LONG_FUSED_T
+#define CSA_BWD_LONG_FUSED_T 1
 #endif
 // Long-window backward: windows of at least this many slots give each warp 16
 // slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
 #ifndef CSA_BWD_LONG_KPT16_FROM
-#define CSA_BWD_LONG_KPT16_FROM 256
+#define CSA_BWD_LONG_KPT16_FROM 128
 #endif
 
 // Long window (W >= 16): blockDim = (32, NCH) with NCH = W / KPT (KPT = 8
@@ -66,6 +72,21 @@ struct ColVec<2> {
   static __device__ __forceinline__ T zero() { return 0u; }
   static __device__ __forceinline__ T ninf() { return kNegInfBf16x2; }
   static __device__ __forceinline__ T pack(const float* x) { return pack_bf16x2(x[0], x[1]); }
+  // VC consecutive floats of shared memory (8-byte aligned)
+  static __device__ __forceinline__ void load_f(const float* p, float* x) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x;
+    x[1] = v.y;
+  }
+  static __device__ __forceinline__ void store_f(float* p, const float* x) {
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+  }
+  static __device__ __forceinline__ void add_f(float* p, const float* x) {
+    float2 v = *reinterpret_cast<float2*>(p);
+    v.x = __fadd_rn(v.x, x[0]);
+    v.y = __fadd_rn(v.y, x[1]);
+    *reinterpret_cast<float2*>(p) = v;
+  }
 };
 template <>
 struct ColVec<4> {
@@ -78,6 +99,25 @@ struct ColVec<4> {
   static __device__ __forceinline__ T pack(const float* x) {
     return make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
   }
+  // VC consecutive floats of shared memory (16-byte aligned)
+  static __device__ __forceinline__ void load_f(const float* p, float* x) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  }
+  static __device__ __forceinline__ void store_f(float* p, const float* x) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  }
+  static __device__ __forceinline__ void add_f(float* p, const float* x) {
+    float4 v = *reinterpret_cast<float4*>(p);
+    v.x = __fadd_rn(v.x, x[0]);
+    v.y = __fadd_rn(v.y, x[1]);
+    v.z = __fadd_rn(v.z, x[2]);
+    v.w = __fadd_rn(v.w, x[3]);
+    *reinterpret_cast<float4*>(p) = v;
+  }
 };
 
 // fixed-order merge of (max, sum exp, sum (g kv) exp) triples rescaled to the
@@ -88,7 +128,7 @@ __device__ __forceinline__ void merge_max_sum2(float& m, float& s, float& t, flo
   const float kNegInf = __int_as_float(0xff800000);
   const float mn = max_nan(m, mb);
   const float mu = mn == kNegInf ? 0.0f : mn;
-  const float fa = softmax_exp(__fsub_rn(m, mu)), fb = softmax_exp(__fsub_rn(mb, mu));
+  const float fa = CSA_BWD_LONG_EXP(__fsub_rn(m, mu)), fb = CSA_BWD_LONG_EXP(__fsub_rn(mb, mu));
   s = __fadd_rn(__fmul_rn(s, fa), __fmul_rn(sb, fb));
   t = __fadd_rn(__fmul_rn(t, fa), __fmul_rn(tb, fb));
   m = mn;
@@ -126,12 +166,13 @@ bwd_long_kernel(const BwdParams bp) {
   __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
   __shared__ float M_s[TC], D_s[TC], S_s[TC];
   // dape sums of the tile, [W][TC]; each cell belongs to one thread
-  extern __shared__ float dacc_s[];
-  float* dacc_t = dacc_s + k0 * TC + lane * VC;
+  extern __shared__ __align__(16) float dacc_s[];
+  float* dacc_t = dacc_s + k0 * TC + lane * VC;  // 8 (VC 2) or 16 (VC 4) byte aligned
 #pragma unroll
-  for (int t = 0; t < KPT; ++t)
-#pragma unroll
-    for (int c = 0; c < VC; ++c) dacc_t[t * TC + c] = 0.0f;
+  for (int t = 0; t < KPT; ++t) {
+    const float z[VC] = {};
+    V::store_f(dacc_t + t * TC, z);
+  }
 
   // this thread's APE values (slots k0.., columns j0..) are re-read per row through L1
   const float* ape_t = p.ape + (int64_t)S::ape_row(k0) * ld + S::half(k0) * d + j0;
@@ -165,8 +206,9 @@ bwd_long_kernel(const BwdParams bp) {
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
   int64_t b = blockIdx.y;
   RowInfo ri{};
+  int hint = 0;  // segment of the last row looked up (rows only increase)
   if (b < true_rows) {
-    ri = row_info(p.cu, p.cuc, p.nseq, b, true_rows, R);
+    ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     loads(b, ri, kvw, gw);
   }
   for (; b < true_rows;) {
@@ -203,7 +245,11 @@ bwd_long_kernel(const BwdParams bp) {
         for (int t = 0; t < KPT; ++t) {
           pz[t][c] = CSA_BWD_LONG_EXP(__fsub_rn(pz[t][c], mu));
           sum = __fadd_rn(sum, pz[t][c]);
+#if CSA_BWD_LONG_FUSED_T
+          tsum = __fmaf_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c], tsum);
+#else
           tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c]));
+#endif
         }
         mloc[c] = m;
         m_s[y * LDS + lane * VC + c] = m;
@@ -216,7 +262,7 @@ bwd_long_kernel(const BwdParams bp) {
     RowInfo rn{};
     typename V::T kvn[KPT], gn = V::zero();
     if (bn < true_rows) {
-      rn = row_info(p.cu, p.cuc, p.nseq, bn, true_rows, R);
+      rn = row_info_from(p.cu, p.cuc, p.nseq, bn, true_rows, R, hint);
       loads(bn, rn, kvn, gn);
     }
     if (compute) {
@@ -246,7 +292,7 @@ bwd_long_kernel(const BwdParams bp) {
         const float den = D_s[lane * VC + c];
         const float mu = M == kNegInf ? 0.0f : M;
         const float ml = mloc[c] == kNegInf ? 0.0f : mloc[c];
-        const float f = softmax_exp(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
+        const float f = CSA_BWD_LONG_EXP(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
         // one scale per column and chunk: f / den (no per-element division;
         // like the exp above, not correctly rounded)
         const float fy = __fmul_rn(f, __frcp_rn(den));
@@ -263,8 +309,8 @@ bwd_long_kernel(const BwdParams bp) {
         for (int c = 0; c < VC; ++c) {
           dz[c] = __fmul_rn(pz[t][c], __fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]));
           dk[c] = __fmul_rn(g[c], pz[t][c]);
-          dacc_t[t * TC + c] = __fadd_rn(dacc_t[t * TC + c], dz[c]);
         }
+        V::add_f(dacc_t + t * TC, dz);
         if (active) {
           V::store(bp.dkv + off + t * ld, V::pack(dk));
           V::store(bp.dscore + off + t * ld, V::pack(dz));
@@ -317,11 +363,13 @@ bwd_long_kernel(const BwdParams bp) {
     float* part = bp.partial + (int64_t)blockIdx.y * (R * ld) + (int64_t)S::ape_row(k0) * ld +
                   S::half(k0) * d + j0;
 #pragma unroll
-    for (int t = 0; t < KPT; ++t)
+    for (int t = 0; t < KPT; ++t) {
+      float v[VC];
+      V::load_f(dacc_t + t * TC, v);
 #pragma unroll
       for (int c = 0; c < VC; c += 2)
-        *reinterpret_cast<float2*>(part + t * ld + c) =
-            make_float2(dacc_t[t * TC + c], dacc_t[t * TC + c + 1]);
+        *reinterpret_cast<float2*>(part + t * ld + c) = make_float2(v[c], v[c + 1]);
+    }
   }
 }
 
