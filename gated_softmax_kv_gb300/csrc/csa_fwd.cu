@@ -30,8 +30,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "csa_device.cuh"
@@ -199,10 +201,24 @@ cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
 }
 
 int occupancy(const void* kernel, int threads, size_t smem) {
+  // cached per (kernel, device, block size, shared memory): the grids of a
+  // call depend on it and the query costs host time on every call otherwise
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const auto key = std::make_tuple(kernel, dev, threads, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
   int blocks = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess ||
       blocks < 1)
-    blocks = 1;
+    return 1;  // not cached: a failed query is retried next time
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = blocks;
   return blocks;
 }
 
