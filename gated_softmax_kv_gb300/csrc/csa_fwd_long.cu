@@ -31,11 +31,17 @@ namespace {
 // same token row (256 bytes per warp per slot). The APE tile of the CTA (W
 // slots x 128 columns) is read through L1, where it stays for the rows the
 // CTA visits.
-constexpr int kLongRows = 8;  // warps per CTA
-constexpr int kBatch = 8;     // window slots per batch
+#ifndef CSA_FWD_LONG_BATCH
+#define CSA_FWD_LONG_BATCH 8
+#endif
+#ifndef CSA_FWD_LONG_MIN_BLOCKS
+#define CSA_FWD_LONG_MIN_BLOCKS 2
+#endif
+constexpr int kLongRows = 8;                   // warps per CTA
+constexpr int kBatch = CSA_FWD_LONG_BATCH;     // window slots per batch
 
 template <int R, int COFF, int D>
-__global__ void __launch_bounds__(32 * kLongRows, 2)
+__global__ void __launch_bounds__(32 * kLongRows, CSA_FWD_LONG_MIN_BLOCKS)
 fwd_long_kernel(const FwdParams f, const int split) {
   grid_dependency_wait();
   allow_dependent_launch();
