@@ -247,21 +247,28 @@ bwd_small_kernel(const BwdParams bp) {
 
 // dape[e] = sum over groups g of partial[g][e] in two fixed levels. A lane
 // owns 4 consecutive elements (16-byte loads; every group row starts on a
-// 32-byte boundary because ratio * coff * d is a multiple of 8). Lane y of the
-// blockDim.y lanes that share those elements sums groups y, y + Y, y + 2Y, ...
-// in ascending order (loads issued 8 at a time so they overlap), then lane 0
-// adds the Y lane sums in order. Y (a power of two <= 32) is fixed by the
-// launch from n and groups, so the order is the same on every run.
-constexpr int kReduceMaxLanes = 32;
+// 32-byte boundary because ratio * coff * d is a multiple of 8); blockDim.x
+// lanes cover consecutive element vectors and blockDim.y lanes share each
+// vector. Lane y sums groups y, y + Y, y + 2Y, ... in ascending order (loads
+// issued 8 at a time so they overlap), then a fixed tree adds the Y lane sums
+// (y += y + Y/2, y + Y/4, ...). X and Y are powers of two fixed by the launch
+// from n and groups, so the order is the same on every run.
+constexpr int kReduceThreads = 1024;
+constexpr int kReduceMaxLanes = 64;
 
-__global__ void __launch_bounds__(32 * kReduceMaxLanes)
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z),
+                     __fadd_rn(a.w, b.w));
+}
+
+__global__ void __launch_bounds__(kReduceThreads)
 dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n4,
                    float4* __restrict__ dape) {
   grid_dependency_wait();
   allow_dependent_launch();
-  __shared__ float4 red[kReduceMaxLanes][32];
-  const int Y = blockDim.y;
-  const int64_t e = (int64_t)blockIdx.x * 32 + threadIdx.x;
+  __shared__ float4 red[kReduceThreads];
+  const int X = blockDim.x, Y = blockDim.y;
+  const int64_t e = (int64_t)blockIdx.x * X + threadIdx.x;
   float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (e < n4) {
     for (int g0 = threadIdx.y; g0 < groups; g0 += 8 * Y) {
@@ -273,31 +280,20 @@ dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (g0 + i * Y < groups) {
-          s.x = __fadd_rn(s.x, v[i].x);
-          s.y = __fadd_rn(s.y, v[i].y);
-          s.z = __fadd_rn(s.z, v[i].z);
-          s.w = __fadd_rn(s.w, v[i].w);
-        }
+        if (g0 + i * Y < groups) s = add4(s, v[i]);
     }
   }
   if (Y == 1) {
     if (e < n4) dape[e] = s;
     return;
   }
-  red[threadIdx.y][threadIdx.x] = s;
-  __syncthreads();
-  if (threadIdx.y == 0 && e < n4) {
-    float4 t = red[0][threadIdx.x];
-    for (int y = 1; y < Y; ++y) {
-      const float4 u = red[y][threadIdx.x];
-      t.x = __fadd_rn(t.x, u.x);
-      t.y = __fadd_rn(t.y, u.y);
-      t.z = __fadd_rn(t.z, u.z);
-      t.w = __fadd_rn(t.w, u.w);
-    }
-    dape[e] = t;
+  float4* mine = red + threadIdx.y * X + threadIdx.x;
+  *mine = s;
+  for (int h = Y >> 1; h > 0; h >>= 1) {  // Y is uniform over the block
+    __syncthreads();
+    if (threadIdx.y < h) *mine = add4(*mine, mine[h * X]);
   }
+  if (threadIdx.y == 0 && e < n4) dape[e] = *mine;
 }
 
 template <int R, int COFF, int D>
@@ -364,15 +360,17 @@ cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, 
                                cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   const int64_t n4 = n / 4;  // n = ratio * coff * d, a multiple of 8
-  const int64_t blocks = (n4 + 31) / 32;
-  // lanes per element group: about two waves of 2048-thread SMs over the
-  // whole GPU, at most one lane per partial; a constant of the problem (152 is
-  // the SM count of a GB300, fixed here so that the order does not depend on
-  // the device)
+  // Y: lanes per element vector, enough that each issues about one batch of
+  // 8 loads; X: element vectors per block, narrower when there are few
+  // vectors so that about 128+ blocks share the work. Both follow from the
+  // problem (n, groups) alone.
   int lanes = 1;
-  while (lanes < kReduceMaxLanes && lanes * 2 <= groups && blocks * 32 * lanes * 2 <= 2 * 152 * 2048)
-    lanes *= 2;
-  return launch_dependent(dape_reduce_kernel, dim3((unsigned)blocks), dim3(32, lanes), 0, stream,
+  while (lanes < kReduceMaxLanes && (int64_t)lanes * 8 < groups) lanes *= 2;
+  int x = 32;
+  while (x > 4 && (n4 + x - 1) / x < 128) x >>= 1;
+  while (x * lanes > kReduceThreads) lanes >>= 1;
+  const int64_t blocks = (n4 + x - 1) / x;
+  return launch_dependent(dape_reduce_kernel, dim3((unsigned)blocks), dim3(x, lanes), 0, stream,
                           reinterpret_cast<const float4*>(partial), groups, n4,
                           reinterpret_cast<float4*>(dape));
 }
