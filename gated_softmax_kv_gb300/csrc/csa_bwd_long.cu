@@ -13,17 +13,13 @@ namespace csa {
 
 namespace {
 
-// exp of the long-window backward (per-element weights, chunk merges and the
-// rescaling of a chunk to the row max). Windows of 16 slots and more have no
+// exp of the long-window backward. Windows of 16 slots and more have no
 // bitwise target (the page aims at bit identity for ratios 2 and 4 only), so
-// they take the single-rounding softmax_exp_fast.
+// the per-element weights take the single-rounding exp (softmax_exp_fast2,
+// two lanes at a time) and T = sum (g kv) e one FMA per slot; the chunk
+// merges and the rescaling of a chunk to the row max use CSA_BWD_LONG_EXP.
 #ifndef CSA_BWD_LONG_EXP
 #define CSA_BWD_LONG_EXP softmax_exp_fast
-#endif
-// T = sum (g kv) e accumulated with one FMA per slot (default) or a rounded
-// product and an add
-#ifndef CSA_BWD_LONG_FUSED_T
-#define CSA_BWD_LONG_FUSED_T 1
 #endif
 // Long-window backward: windows of at least this many slots give each warp 16
 // slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
@@ -82,10 +78,8 @@ struct ColVec<2> {
     *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
   }
   static __device__ __forceinline__ void add_f(float* p, const float* x) {
-    float2 v = *reinterpret_cast<float2*>(p);
-    v.x = __fadd_rn(v.x, x[0]);
-    v.y = __fadd_rn(v.y, x[1]);
-    *reinterpret_cast<float2*>(p) = v;
+    float2* q = reinterpret_cast<float2*>(p);
+    *q = add2_rn(*q, make_float2(x[0], x[1]));
   }
 };
 template <>
@@ -112,11 +106,9 @@ struct ColVec<4> {
   }
   static __device__ __forceinline__ void add_f(float* p, const float* x) {
     float4 v = *reinterpret_cast<float4*>(p);
-    v.x = __fadd_rn(v.x, x[0]);
-    v.y = __fadd_rn(v.y, x[1]);
-    v.z = __fadd_rn(v.z, x[2]);
-    v.w = __fadd_rn(v.w, x[3]);
-    *reinterpret_cast<float4*>(p) = v;
+    const float2 lo = add2_rn(make_float2(v.x, v.y), make_float2(x[0], x[1]));
+    const float2 hi = add2_rn(make_float2(v.z, v.w), make_float2(x[2], x[3]));
+    *reinterpret_cast<float4*>(p) = make_float4(lo.x, lo.y, hi.x, hi.y);
   }
 };
 
@@ -227,34 +219,45 @@ bwd_long_kernel(const BwdParams bp) {
         for (int c = 0; c < VC; c += 2) {
           const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld + c))
                                   : make_float2(0.0f, 0.0f);
-          pz[t][c] = __fadd_rn(V::elem(scw[t], c), a.x);
-          pz[t][c + 1] = __fadd_rn(V::elem(scw[t], c + 1), a.y);
+          const float2 z =
+              add2_rn(make_float2(V::elem(scw[t], c), V::elem(scw[t], c + 1)), a);
+          pz[t][c] = z.x;
+          pz[t][c + 1] = z.y;
         }
       }
       // phase 1: per column, the chunk's max m_c, e = exp(z - m_c), its sum
       // and T_c = sum (g kv) e; one fixed-order merge of (max, sum, T) then
-      // gives the row's max M, den and S = T / den together
+      // gives the row's max M, den and S = T / den together. Columns go in
+      // pairs through the two-lane fp32 instructions (same roundings).
 #pragma unroll
-      for (int c = 0; c < VC; ++c) {
-        float m = pz[0][c];
+      for (int c = 0; c < VC; c += 2) {
+        float m0 = pz[0][c], m1 = pz[0][c + 1];
 #pragma unroll
-        for (int t = 1; t < KPT; ++t) m = max_nan(m, pz[t][c]);
-        const float mu = m == kNegInf ? 0.0f : m;  // an all -inf chunk contributes 0
-        float sum = 0.0f, tsum = 0.0f;
+        for (int t = 1; t < KPT; ++t) {
+          m0 = max_nan(m0, pz[t][c]);
+          m1 = max_nan(m1, pz[t][c + 1]);
+        }
+        // an all -inf chunk contributes 0
+        const float2 mu = make_float2(m0 == kNegInf ? 0.0f : m0, m1 == kNegInf ? 0.0f : m1);
+        const float2 g2 = make_float2(g[c], g[c + 1]);
+        float2 sum = make_float2(0.0f, 0.0f), tsum = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int t = 0; t < KPT; ++t) {
-          pz[t][c] = CSA_BWD_LONG_EXP(__fsub_rn(pz[t][c], mu));
-          sum = __fadd_rn(sum, pz[t][c]);
-#if CSA_BWD_LONG_FUSED_T
-          tsum = __fmaf_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c], tsum);
-#else
-          tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), pz[t][c]));
-#endif
+          const float2 e = softmax_exp_fast2(sub2_rn(make_float2(pz[t][c], pz[t][c + 1]), mu));
+          pz[t][c] = e.x;
+          pz[t][c + 1] = e.y;
+          sum = add2_rn(sum, e);
+          const float2 dp = mul2_rn(g2, make_float2(V::elem(kvw[t], c), V::elem(kvw[t], c + 1)));
+          tsum = fma2_rn(dp, e, tsum);
         }
-        mloc[c] = m;
-        m_s[y * LDS + lane * VC + c] = m;
-        d_s[y * LDS + lane * VC + c] = sum;
-        s_s[y * LDS + lane * VC + c] = tsum;
+        mloc[c] = m0;
+        mloc[c + 1] = m1;
+        m_s[y * LDS + lane * VC + c] = m0;
+        m_s[y * LDS + lane * VC + c + 1] = m1;
+        d_s[y * LDS + lane * VC + c] = sum.x;
+        d_s[y * LDS + lane * VC + c + 1] = sum.y;
+        s_s[y * LDS + lane * VC + c] = tsum.x;
+        s_s[y * LDS + lane * VC + c + 1] = tsum.y;
       }
     }
     // prefetch the next row of this CTA
@@ -286,6 +289,7 @@ bwd_long_kernel(const BwdParams bp) {
       }
       __syncthreads();
       // phase 2: p = e exp(m_c - M) / den, dscore = p (g kv - S), dkv = g p
+      float fy[VC], Sv[VC];
 #pragma unroll
       for (int c = 0; c < VC; ++c) {
         const float M = M_s[lane * VC + c];
@@ -295,20 +299,23 @@ bwd_long_kernel(const BwdParams bp) {
         const float f = CSA_BWD_LONG_EXP(__fsub_rn(ml, mu));  // rescales this chunk's e to the row max
         // one scale per column and chunk: f / den (no per-element division;
         // like the exp above, not correctly rounded)
-        const float fy = __fmul_rn(f, __frcp_rn(den));
-#pragma unroll
-        for (int t = 0; t < KPT; ++t) pz[t][c] = __fmul_rn(pz[t][c], fy);
+        fy[c] = __fmul_rn(f, __frcp_rn(den));
+        Sv[c] = S_s[lane * VC + c];
       }
-      float Sv[VC];
-#pragma unroll
-      for (int c = 0; c < VC; ++c) Sv[c] = S_s[lane * VC + c];
 #pragma unroll
       for (int t = 0; t < KPT; ++t) {
         float dz[VC], dk[VC];
 #pragma unroll
-        for (int c = 0; c < VC; ++c) {
-          dz[c] = __fmul_rn(pz[t][c], __fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]));
-          dk[c] = __fmul_rn(g[c], pz[t][c]);
+        for (int c = 0; c < VC; c += 2) {
+          const float2 g2 = make_float2(g[c], g[c + 1]);
+          const float2 pp = mul2_rn(make_float2(pz[t][c], pz[t][c + 1]), make_float2(fy[c], fy[c + 1]));
+          const float2 dp = mul2_rn(g2, make_float2(V::elem(kvw[t], c), V::elem(kvw[t], c + 1)));
+          const float2 z = mul2_rn(pp, sub2_rn(dp, make_float2(Sv[c], Sv[c + 1])));
+          const float2 k = mul2_rn(g2, pp);
+          dz[c] = z.x;
+          dz[c + 1] = z.y;
+          dk[c] = k.x;
+          dk[c + 1] = k.y;
         }
         V::add_f(dacc_t + t * TC, dz);
         if (active) {

@@ -80,6 +80,42 @@ __device__ __forceinline__ float softmax_exp_fast(float x) {
   return ex2_approx_ftz(__fmul_rn(x, __int_as_float(0x3fb8aa3b)));
 }
 
+// ---- paired fp32 arithmetic --------------------------------------------------
+
+// Two independent fp32 operations in one instruction (the f32x2 forms of the
+// sm_100 family). Each lane is rounded to nearest exactly as __fadd_rn /
+// __fsub_rn / __fmul_rn / __fmaf_rn would round it, so the results are
+// bit-identical to the scalar operations; only the instruction count halves.
+#define CSA_F32X2_OP(NAME, OP)                                                              \
+  __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                              \
+    float2 r;                                                                               \
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" OP \
+        " d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"                                            \
+        : "=f"(r.x), "=f"(r.y)                                                              \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                          \
+    return r;                                                                               \
+  }
+CSA_F32X2_OP(add2_rn, "add.rn.f32x2")
+CSA_F32X2_OP(sub2_rn, "sub.rn.f32x2")
+CSA_F32X2_OP(mul2_rn, "mul.rn.f32x2")
+#undef CSA_F32X2_OP
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// softmax_exp_fast on two lanes: the products x * log2 e in one instruction.
+__device__ __forceinline__ float2 softmax_exp_fast2(float2 x) {
+  const float l = __int_as_float(0x3fb8aa3b);
+  const float2 t = mul2_rn(x, make_float2(l, l));
+  return make_float2(ex2_approx_ftz(t.x), ex2_approx_ftz(t.y));
+}
+
 // ---- division ---------------------------------------------------------------
 
 // a / b rounded to nearest from y = RN(1/b): q = RN(a*y), then one
