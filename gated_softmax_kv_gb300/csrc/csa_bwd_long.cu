@@ -78,8 +78,10 @@ struct ColVec<2> {
     *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
   }
   static __device__ __forceinline__ void add_f(float* p, const float* x) {
-    float2* q = reinterpret_cast<float2*>(p);
-    *q = add2_rn(*q, make_float2(x[0], x[1]));
+    float2 v = *reinterpret_cast<float2*>(p);
+    v.x = __fadd_rn(v.x, x[0]);
+    v.y = __fadd_rn(v.y, x[1]);
+    *reinterpret_cast<float2*>(p) = v;
   }
 };
 template <>
@@ -106,9 +108,11 @@ struct ColVec<4> {
   }
   static __device__ __forceinline__ void add_f(float* p, const float* x) {
     float4 v = *reinterpret_cast<float4*>(p);
-    const float2 lo = add2_rn(make_float2(v.x, v.y), make_float2(x[0], x[1]));
-    const float2 hi = add2_rn(make_float2(v.z, v.w), make_float2(x[2], x[3]));
-    *reinterpret_cast<float4*>(p) = make_float4(lo.x, lo.y, hi.x, hi.y);
+    v.x = __fadd_rn(v.x, x[0]);
+    v.y = __fadd_rn(v.y, x[1]);
+    v.z = __fadd_rn(v.z, x[2]);
+    v.w = __fadd_rn(v.w, x[3]);
+    *reinterpret_cast<float4*>(p) = v;
   }
 };
 
@@ -307,10 +311,14 @@ bwd_long_kernel(const BwdParams bp) {
         float dz[VC], dk[VC];
 #pragma unroll
         for (int c = 0; c < VC; c += 2) {
+          // a two-lane product is never followed by a two-lane add or
+          // subtract (the compiler may fuse such a pair): dp - S stays scalar
           const float2 g2 = make_float2(g[c], g[c + 1]);
           const float2 pp = mul2_rn(make_float2(pz[t][c], pz[t][c + 1]), make_float2(fy[c], fy[c + 1]));
-          const float2 dp = mul2_rn(g2, make_float2(V::elem(kvw[t], c), V::elem(kvw[t], c + 1)));
-          const float2 z = mul2_rn(pp, sub2_rn(dp, make_float2(Sv[c], Sv[c + 1])));
+          const float2 diff =
+              make_float2(__fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]),
+                          __fsub_rn(__fmul_rn(g[c + 1], V::elem(kvw[t], c + 1)), Sv[c + 1]));
+          const float2 z = mul2_rn(pp, diff);
           const float2 k = mul2_rn(g2, pp);
           dz[c] = z.x;
           dz[c + 1] = z.y;

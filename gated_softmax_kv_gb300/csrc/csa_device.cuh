@@ -84,8 +84,10 @@ __device__ __forceinline__ float softmax_exp_fast(float x) {
 
 // Two independent fp32 operations in one instruction (the f32x2 forms of the
 // sm_100 family). Each lane is rounded to nearest exactly as __fadd_rn /
-// __fsub_rn / __fmul_rn / __fmaf_rn would round it, so the results are
-// bit-identical to the scalar operations; only the instruction count halves.
+// __fsub_rn / __fmul_rn / __fmaf_rn would round it. Unlike the scalar _rn
+// forms, a two-lane product followed by a two-lane add or subtract may be
+// fused into one FMA by the compiler (measured), so callers never chain them
+// that way; every other use gives the scalar bits with half the instructions.
 #define CSA_F32X2_OP(NAME, OP)                                                              \
   __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                              \
     float2 r;                                                                               \

@@ -27,7 +27,37 @@ __global__ void div_kernel(const float* __restrict__ a, const float* __restrict_
     q[i] = csa::div_rn_by_rcp(a[i], b[i], __frcp_rn(b[i]));
 }
 
+// The two-lane fp32 helpers one operation at a time (every result stored, so
+// nothing can be fused), in the chains the kernels use (a product feeding a
+// product, a difference feeding a product, an FMA), and the scalar FMA.
+__global__ void pair_ops_kernel(const float2* __restrict__ a, const float2* __restrict__ b,
+                                const float2* __restrict__ c, float2* __restrict__ out,
+                                int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float2 x = a[i], y = b[i], z = c[i];
+    out[0 * n + i] = csa::add2_rn(x, y);
+    out[1 * n + i] = csa::sub2_rn(x, z);
+    out[2 * n + i] = csa::mul2_rn(y, z);
+    out[3 * n + i] = csa::mul2_rn(csa::mul2_rn(x, y), z);
+    out[4 * n + i] = csa::mul2_rn(csa::sub2_rn(x, y), z);
+    out[5 * n + i] = csa::fma2_rn(x, y, z);
+    out[6 * n + i] = make_float2(__fmaf_rn(x.x, y.x, z.x), __fmaf_rn(x.y, y.y, z.y));
+  }
+}
+
 }  // namespace
+
+extern "C" int32_t csa_selftest_pair_ops(const float* a, const float* b, const float* c,
+                                         float* out, int64_t n_pairs, cudaStream_t stream) {
+  if (n_pairs <= 0) return 0;
+  int64_t blocks = (n_pairs + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  pair_ops_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      reinterpret_cast<const float2*>(a), reinterpret_cast<const float2*>(b),
+      reinterpret_cast<const float2*>(c), reinterpret_cast<float2*>(out), n_pairs);
+  return (int32_t)cudaGetLastError();
+}
 
 extern "C" int32_t csa_selftest_div(const float* a, const float* b, float* q, int64_t n,
                                     cudaStream_t stream) {

@@ -122,3 +122,41 @@ def test_forward_fast_exp_error_bound():
     assert lib.csa_selftest_softmax_exp_fast(sp.data_ptr(), out.data_ptr(), 2, None) == 0
     o = out.cpu().numpy()
     assert o[0] == 0.0 and np.isnan(o[1])
+
+
+def test_two_lane_fp32_ops_round_like_scalar():
+    """The f32x2 helpers of the kernels (add/sub/mul/fma .rn.f32x2) against
+    numpy's fp32 arithmetic, one rounding per operation: each alone, a product
+    feeding a product, a difference feeding a product, and the two-lane FMA
+    against the scalar FMA. (A product feeding an add or a subtract may be
+    fused by the compiler; the kernels never chain them that way.) Random
+    operands over wide exponent ranges plus signed zeros, infinities, NaN and
+    subnormals."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    lib.csa_selftest_pair_ops.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64, ctypes.c_void_p]
+    lib.csa_selftest_pair_ops.restype = ctypes.c_int32
+    rng = np.random.default_rng(7)
+    n = 1 << 20
+    def draw():
+        m = rng.standard_normal(n).astype(np.float32)
+        e = rng.integers(-20, 21, n).astype(np.float32)
+        return (m * np.exp2(e)).astype(np.float32)
+    a, b, c = draw(), draw(), draw()
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-40, -3e-39, 3.4e38], np.float32)
+    a[:8], b[8:16], c[16:24] = special, special, special
+    dev = [torch.from_numpy(x).cuda() for x in (a, b, c)]
+    out = torch.empty(7 * n, dtype=torch.float32, device="cuda")
+    assert lib.csa_selftest_pair_ops(*(t.data_ptr() for t in dev), out.data_ptr(), n // 2, None) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().reshape(7, n)
+    with np.errstate(all="ignore"):
+        want = [a + b, a - c, b * c, (a * b) * c, (a - b) * c]  # numpy fp32: one rounding per step
+    for row, w in enumerate(want):
+        same = (got[row].view(np.uint32) == w.view(np.uint32)) | (np.isnan(got[row]) & np.isnan(w))
+        assert same.all(), f"pattern {row}: {int((~same).sum())} differ"
+    same = (got[5].view(np.uint32) == got[6].view(np.uint32)) | (np.isnan(got[5]) & np.isnan(got[6]))
+    assert same.all(), f"fma2: {int((~same).sum())} differ from the scalar FMA"
