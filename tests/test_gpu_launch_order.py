@@ -68,3 +68,49 @@ def test_backward_consumes_the_forward_output_in_stream_order(gsk, name):
     chained = run(sync=False)
     for a, b, what in zip(ordered, chained, ("second out", "dkv", "dscore", "dape")):
         assert np.array_equal(a, b), what
+
+
+def test_two_host_threads_on_two_streams(gsk):
+    """Two host threads, each on its own stream, run forward + backward on
+    different inputs at the same time, several times over: the library's
+    shared state (the dape workspace pool, the occupancy and shared-memory
+    caches) is behind locks and each call's workspace is stream-ordered, so
+    every result equals the same calls made alone."""
+    import threading
+    cases = [workloads.config("r4d512"), workloads.config("r128c1")]
+
+    def upload(case):
+        return dict(kv=_bf16(case.kv), score=_bf16(case.score), go=_bf16(case.grad_out),
+                    ape=torch.from_numpy(case.ape).cuda(), cu=torch.from_numpy(case.cu_seqlens).cuda(),
+                    cuc=torch.from_numpy(case.cu_seqlens_comp).cuda())
+
+    dev = [upload(c) for c in cases]
+    torch.cuda.synchronize()  # the uploads ran on the default stream
+
+    def run(i, stream):
+        c, t = cases[i], dev[i]
+        meta = (c.capacity, c.ratio, c.coff, c.head_dim)
+        with torch.cuda.stream(stream):
+            out = gsk.csa_compress_fwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], *meta,
+                                       stream=stream)
+            dkv, ds, dape = gsk.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
+                                                 *meta, t["go"], stream=stream)
+        stream.synchronize()
+        return [_bits(x) for x in (out, dkv, ds, dape)]
+
+    alone = [run(i, torch.cuda.Stream()) for i in range(2)]
+    results = {}
+
+    def worker(i):
+        s = torch.cuda.Stream()
+        results[i] = [run(i, s) for _ in range(4)]
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    for i in range(2):
+        for rep in results[i]:
+            for a, b in zip(alone[i], rep):
+                assert np.array_equal(a, b)
