@@ -23,11 +23,6 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_at(uint32_t w, int h) { return h ? bf16_hi(w) : bf16_lo(w); }
 
-// Element c (0..7) of a 16-byte vector of bf16.
-__device__ __forceinline__ float bf16_elem(const uint4& v, int c) {
-  const uint32_t w = (c >> 1) == 0 ? v.x : (c >> 1) == 1 ? v.y : (c >> 1) == 2 ? v.z : v.w;
-  return bf16_at(w, c & 1);
-}
 
 // Two fp32 values -> one bf16x2 word (lo at the lower address), nearest-even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -184,39 +179,13 @@ struct RowInfo {
   bool last;         // last block of its segment
 };
 
-// Row b < true_rows: s = last segment with cu_seqlens_comp[s] <= b (binary
-// search; terminates and stays in [0, num_seqs) whatever the array holds),
+// Row b < true_rows: s = last segment with cu_seqlens_comp[s] <= b,
 // i = b - cu_seqlens_comp[s], base = cu_seqlens[s] + i * ratio.
 // Row b >= true_rows (static-capacity padding): first block from token 0.
-__device__ __forceinline__ RowInfo row_info(const int32_t* __restrict__ cu,
-                                            const int32_t* __restrict__ cuc, int nseq,
-                                            int64_t b, int64_t true_rows, int ratio) {
-  RowInfo ri;
-  if (b >= true_rows) {
-    ri.base = 0;
-    ri.seg_end = 0;
-    ri.first = true;
-    ri.last = false;
-    return ri;
-  }
-  int lo = 0, hi = nseq;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((int64_t)__ldg(cuc + mid) <= b) lo = mid; else hi = mid;
-  }
-  const int64_t c0 = __ldg(cuc + lo);
-  const int64_t c1 = __ldg(cuc + lo + 1);
-  const int64_t i = b - c0;
-  ri.base = (int64_t)__ldg(cu + lo) + i * ratio;
-  ri.seg_end = __ldg(cu + lo + 1);
-  ri.first = (i == 0);
-  ri.last = (i == c1 - c0 - 1);
-  return ri;
-}
-
-// Same map for a thread that visits rows in increasing order: `hint` is a
-// segment with cu_seqlens_comp[hint] <= b from an earlier row (0 at first);
-// the common case costs one load.
+// For a thread that visits rows in increasing order: `hint` is a segment with
+// cu_seqlens_comp[hint] <= b from an earlier row (0 at first); the common case
+// costs one load, otherwise a binary search over the later segments, which
+// terminates and stays in [0, num_seqs) whatever the arrays hold.
 __device__ __forceinline__ RowInfo row_info_from(const int32_t* __restrict__ cu,
                                                  const int32_t* __restrict__ cuc, int nseq,
                                                  int64_t b, int64_t true_rows, int ratio,
