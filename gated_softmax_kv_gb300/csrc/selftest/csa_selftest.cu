@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "csa_device.cuh"
+#include "csa_exp_cr.cuh"
 
 namespace {
 
@@ -46,7 +47,24 @@ __global__ void pair_ops_kernel(const float2* __restrict__ a, const float2* __re
   }
 }
 
+__global__ void exp_cr_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  __shared__ float2 tab[csa::kExpTableSize];
+  csa::exp_cr_table(tab);
+  __syncthreads();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = csa::exp_cr(x[i], tab);
+}
+
 }  // namespace
+
+extern "C" int32_t csa_selftest_exp_cr(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return 0;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  exp_cr_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, n);
+  return (int32_t)cudaGetLastError();
+}
 
 extern "C" int32_t csa_selftest_pair_ops(const float* a, const float* b, const float* c,
                                          float* out, int64_t n_pairs, cudaStream_t stream) {

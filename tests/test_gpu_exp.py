@@ -160,3 +160,35 @@ def test_two_lane_fp32_ops_round_like_scalar():
         assert same.all(), f"pattern {row}: {int((~same).sum())} differ"
     same = (got[5].view(np.uint32) == got[6].view(np.uint32)) | (np.isnan(got[5]) & np.isnan(got[6]))
     assert same.all(), f"fma2: {int((~same).sum())} differ from the scalar FMA"
+
+
+def test_correctly_rounded_exp_matches_the_oracle():
+    """exp_cr (the exact mode's exp) against the oracle's exp (fp64 exp rounded
+    once to fp32), bit for bit: every 61st fp32 value in [-86, 0] (the
+    table-driven path and its rounding test), a dense sweep of [-1, 0],
+    [-104, -86] (the fp64 path, down through the subnormals to 0) and the
+    special values."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    lib.csa_selftest_exp_cr.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.c_void_p]
+    lib.csa_selftest_exp_cr.restype = ctypes.c_int32
+    lo, hi = np.float32(-86.0).view(np.uint32), np.uint32(0x80000000)
+    xs = np.concatenate([
+        np.arange(hi, lo, 61, dtype=np.uint64).astype(np.uint32).view(np.float32),
+        np.linspace(-1.0, 0.0, 1 << 22, dtype=np.float32),
+        np.linspace(-104.0, -86.0, 1 << 20, dtype=np.float32),
+        np.array([0.0, -0.0, -np.inf, np.nan, -86.0, -87.0, -103.97, -1e-30], np.float32)])
+    x_d = torch.from_numpy(xs).cuda()
+    y_d = torch.empty_like(x_d)
+    assert lib.csa_selftest_exp_cr(x_d.data_ptr(), y_d.data_ptr(), xs.size, None) == 0
+    torch.cuda.synchronize()
+    got = y_d.cpu().numpy()
+    want = oracle.exp_f32_array(xs)
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    bad = np.nonzero(~same)[0]
+    detail = [(float(xs[i]), float(got[i]), float(want[i])) for i in bad[:8]]
+    assert bad.size == 0, f"{bad.size} of {xs.size} differ (x, got, want): {detail}"
