@@ -49,6 +49,9 @@ def parse():
                          "r128c1, or a pack `pack-r{ratio}c{coff}d{head_dim}-{n}x{len}`")
     ap.add_argument("--graph", action="store_true",
                     help="also time one forward + backward step captured in a CUDA graph and replayed")
+    ap.add_argument("--exact", action="store_true",
+                    help="time the exact mode (csa_compress_fwd_exact / csa_compress_bwd_exact; "
+                         "windows of at most 8 slots)")
     ap.add_argument("--l2", choices=["auto", "flush", "warm"], default="auto",
                     help="flush L2 before every call (auto: when kv + score fit in twice the L2)")
     args = ap.parse_args()
@@ -376,10 +379,11 @@ def run_e2e(args, case, dev, stream, ranks):
         if used[s]:
             stream.wait_event(ev["out"][s])       # step i-2's results have left this set
         gsk.csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
-                                 cuc.data_ptr(), case.num_seqs, T, C, r, coff, d, out.data_ptr(), sh)
+                                 cuc.data_ptr(), case.num_seqs, T, C, r, coff, d, out.data_ptr(), sh,
+                                 args.exact)
         gsk.csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
                                  cuc.data_ptr(), case.num_seqs, T, C, r, coff, d, go.data_ptr(),
-                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh)
+                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), sh, args.exact)
         ev["comp"][s].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev["comp"][s])
@@ -472,12 +476,12 @@ def run_gpu(args, rank, world, local):
 
     def fwd_g(h):
         gsk.csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
-                                 cuc.data_ptr(), nseq, T, C, r, coff, d, out.data_ptr(), h)
+                                 cuc.data_ptr(), nseq, T, C, r, coff, d, out.data_ptr(), h, args.exact)
 
     def bwd_g(h):
         gsk.csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu.data_ptr(),
                                  cuc.data_ptr(), nseq, T, C, r, coff, d, grad_out.data_ptr(),
-                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), h)
+                                 dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(), h, args.exact)
 
     def fwd():
         fwd_g(sh)
@@ -554,7 +558,9 @@ def run_gpu(args, rank, world, local):
     value = T * K * world / elapsed
     dominant = "bwd" if bwd_avg >= fwd_avg else "fwd"
     dom_bytes, dom_gbs = (bwd_bytes, bwd_gbs) if dominant == "bwd" else (fwd_bytes, fwd_gbs)
-    traffic = ncu_traffic("csa_compress_bwd" if dominant == "bwd" else "csa_compress_fwd", T)
+    # the recorded DRAM counters were taken on the default mode's kernels
+    traffic = None if args.exact else \
+        ncu_traffic("csa_compress_bwd" if dominant == "bwd" else "csa_compress_fwd", T)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -573,7 +579,8 @@ def run_gpu(args, rank, world, local):
                           "per-call events); value from the summed call times") if flush else
                          (f"inputs larger than L2 (kv+score {in_bytes / 2**20:.0f} MiB per step), no flush"
                           if in_bytes >= 2 * L2_BYTES else "L2 warm between calls (--l2 warm)"),
-                   "step": "csa_compress_fwd + csa_compress_bwd (3 kernels)"},
+                   "step": ("csa_compress_fwd_exact + csa_compress_bwd_exact (3 kernels)" if args.exact
+                            else "csa_compress_fwd + csa_compress_bwd (3 kernels)")},
         "roofline": {"bound": "hbm", "kernel": "csa_compress_" + dominant + (" (bwd kernel + dape reduce)" if dominant == "bwd" else ""),
                      "achieved": dom_gbs, "peak": peak, "unit": "GB/s", "frac": dom_gbs / peak,
                      "traffic": traffic, "algorithmic_bytes": dom_bytes, "peak_source": peak_src},

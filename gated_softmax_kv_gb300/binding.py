@@ -43,6 +43,10 @@ def load() -> ctypes.CDLL:
     lib.csa_compress_fwd.restype = ctypes.c_int
     lib.csa_compress_bwd.argtypes = common + [vp, vp, vp, vp, vp]
     lib.csa_compress_bwd.restype = ctypes.c_int
+    lib.csa_compress_fwd_exact.argtypes = common + [vp, vp]
+    lib.csa_compress_fwd_exact.restype = ctypes.c_int
+    lib.csa_compress_bwd_exact.argtypes = common + [vp, vp, vp, vp, vp]
+    lib.csa_compress_bwd_exact.restype = ctypes.c_int
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_cuda_error.argtypes = []
@@ -64,9 +68,11 @@ def _raise(status: int):
 
 def csa_compress_fwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seqlens_comp: int,
                          num_seqs: int, total_tokens: int, capacity: int, ratio: int, coff: int,
-                         head_dim: int, out: int, stream: int = 0) -> None:
-    st = load().csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs,
-                                 total_tokens, capacity, ratio, coff, head_dim, out, stream)
+                         head_dim: int, out: int, stream: int = 0, exact: bool = False) -> None:
+    lib = load()
+    fn = lib.csa_compress_fwd_exact if exact else lib.csa_compress_fwd
+    st = fn(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity, ratio,
+            coff, head_dim, out, stream)
     if st != 0:
         _raise(st)
 
@@ -74,10 +80,11 @@ def csa_compress_fwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seql
 def csa_compress_bwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seqlens_comp: int,
                          num_seqs: int, total_tokens: int, capacity: int, ratio: int, coff: int,
                          head_dim: int, grad_out: int, dkv: int, dscore: int, dape: int,
-                         stream: int = 0) -> None:
-    st = load().csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs,
-                                 total_tokens, capacity, ratio, coff, head_dim, grad_out, dkv,
-                                 dscore, dape, stream)
+                         stream: int = 0, exact: bool = False) -> None:
+    lib = load()
+    fn = lib.csa_compress_bwd_exact if exact else lib.csa_compress_bwd
+    st = fn(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity, ratio,
+            coff, head_dim, grad_out, dkv, dscore, dape, stream)
     if st != 0:
         _raise(st)
 
@@ -124,8 +131,9 @@ def _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim):
 
 
 def csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int, ratio: int,
-                     coff: int, head_dim: int, out=None, stream=None):
-    """Forward on device tensors; returns out [capacity, head_dim] bf16."""
+                     coff: int, head_dim: int, out=None, stream=None, exact: bool = False):
+    """Forward on device tensors; returns out [capacity, head_dim] bf16.
+    exact=True calls csa_compress_fwd_exact (windows of at most 8 slots)."""
     import torch
     dev, nseq, T = _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim)
     if out is None:
@@ -135,15 +143,16 @@ def csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int,
         raise ValueError("out must be [capacity, head_dim]")
     csa_compress_fwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu_seqlens.data_ptr(),
                          cu_seqlens_comp.data_ptr(), nseq, T, capacity, ratio, coff, head_dim,
-                         out.data_ptr(), _stream_handle(stream, dev))
+                         out.data_ptr(), _stream_handle(stream, dev), exact)
     return out
 
 
 def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int, ratio: int,
                      coff: int, head_dim: int, grad_out, dkv=None, dscore=None, dape=None,
-                     stream=None):
+                     stream=None, exact: bool = False):
     """Backward on device tensors; returns (dkv, dscore, dape). dkv/dscore may be
-    uninitialised; dape is overwritten."""
+    uninitialised; dape is overwritten. exact=True calls csa_compress_bwd_exact
+    (windows of at most 8 slots)."""
     import torch
     dev, nseq, T = _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim)
     _check(grad_out, "grad_out", torch.bfloat16, dev, 2)
@@ -163,7 +172,7 @@ def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int,
     csa_compress_bwd_ptr(kv.data_ptr(), score.data_ptr(), ape.data_ptr(), cu_seqlens.data_ptr(),
                          cu_seqlens_comp.data_ptr(), nseq, T, capacity, ratio, coff, head_dim,
                          grad_out.data_ptr(), dkv.data_ptr(), dscore.data_ptr(), dape.data_ptr(),
-                         _stream_handle(stream, dev))
+                         _stream_handle(stream, dev), exact)
     return dkv, dscore, dape
 
 

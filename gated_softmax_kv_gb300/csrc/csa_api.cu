@@ -57,6 +57,7 @@ csa::Problem make_problem(const void* kv, const void* score, const float* ape, c
   p.d = head_dim;
   p.T = total_tokens;
   p.C = capacity;
+  p.exact = false;
   return p;
 }
 
@@ -85,6 +86,73 @@ cudaError_t workspace_pool(cudaMemPool_t* out) {
   }
   *out = pools[dev];
   return cudaSuccess;
+}
+
+// Exact mode (csa_compress_fwd_exact / csa_compress_bwd_exact): the
+// small-window shapes only (coff * ratio <= 8).
+bool exact_supported(int32_t ratio, int32_t coff) { return coff * ratio <= 8; }
+
+csa_status_t fwd_call(const void* kv, const void* score, const float* ape, const int32_t* cu_seqlens,
+                      const int32_t* cu_seqlens_comp, int32_t num_seqs, int64_t total_tokens,
+                      int64_t capacity, int32_t ratio, int32_t coff, int32_t head_dim, void* out,
+                      cudaStream_t stream, bool exact) {
+  csa_status_t st = validate(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
+                             capacity, ratio, coff, head_dim);
+  if (st != CSA_OK) return st;
+  if (exact && !exact_supported(ratio, coff)) return CSA_ERR_UNSUPPORTED;
+  if (capacity > 0 && !out) return CSA_ERR_NULL;
+  if (!aligned(out, 16)) return CSA_ERR_ALIGN;
+  if (capacity == 0) return CSA_OK;
+  csa::FwdParams f;
+  f.p = make_problem(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
+                     capacity, ratio, coff, head_dim);
+  f.p.exact = exact;
+  f.out = static_cast<uint16_t*>(out);
+  cudaError_t e = csa::launch_fwd(f, stream);
+  return e == cudaSuccess ? CSA_OK : cuda_fail(e);
+}
+
+csa_status_t bwd_call(const void* kv, const void* score, const float* ape, const int32_t* cu_seqlens,
+                      const int32_t* cu_seqlens_comp, int32_t num_seqs, int64_t total_tokens,
+                      int64_t capacity, int32_t ratio, int32_t coff, int32_t head_dim,
+                      const void* grad_out, void* dkv, void* dscore, float* dape,
+                      cudaStream_t stream, bool exact) {
+  csa_status_t st = validate(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
+                             capacity, ratio, coff, head_dim);
+  if (st != CSA_OK) return st;
+  if (exact && !exact_supported(ratio, coff)) return CSA_ERR_UNSUPPORTED;
+  if ((capacity > 0 && !grad_out) || (total_tokens > 0 && (!dkv || !dscore)) || !dape)
+    return CSA_ERR_NULL;
+  if (!aligned(grad_out, 16) || !aligned(dkv, 16) || !aligned(dscore, 16) || !aligned(dape, 16))
+    return CSA_ERR_ALIGN;
+
+  csa::BwdParams b;
+  b.p = make_problem(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
+                     capacity, ratio, coff, head_dim);
+  b.p.exact = exact;
+  b.grad_out = static_cast<const uint16_t*>(grad_out);
+  b.dkv = static_cast<uint16_t*>(dkv);
+  b.dscore = static_cast<uint16_t*>(dscore);
+  csa::BwdShape shape;
+  cudaError_t e = csa::plan_bwd(b.p, &shape);
+  if (e != cudaSuccess) return cuda_fail(e);
+  b.groups = shape.groups;
+
+  const int64_t n_ape = (int64_t)ratio * coff * head_dim;
+  const size_t ws_bytes = sizeof(float) * (size_t)n_ape * (size_t)shape.groups;
+  cudaMemPool_t pool;
+  e = workspace_pool(&pool);
+  if (e != cudaSuccess) return cuda_fail(e);
+  void* ws = nullptr;
+  e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  b.partial = static_cast<float*>(ws);
+  e = csa::launch_bwd(b, shape, stream);
+  if (e == cudaSuccess) e = csa::launch_dape_reduce(b.partial, shape.groups, n_ape, dape, stream);
+  cudaError_t ef = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (ef != cudaSuccess) return cuda_fail(ef);
+  return CSA_OK;
 }
 
 }  // namespace
@@ -119,18 +187,17 @@ csa_status_t csa_compress_fwd(const void* kv, const void* score, const float* ap
                               int32_t num_seqs, int64_t total_tokens, int64_t capacity,
                               int32_t ratio, int32_t coff, int32_t head_dim, void* out,
                               cudaStream_t stream) {
-  csa_status_t st = validate(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
-                             capacity, ratio, coff, head_dim);
-  if (st != CSA_OK) return st;
-  if (capacity > 0 && !out) return CSA_ERR_NULL;
-  if (!aligned(out, 16)) return CSA_ERR_ALIGN;
-  if (capacity == 0) return CSA_OK;
-  csa::FwdParams f;
-  f.p = make_problem(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
-                     capacity, ratio, coff, head_dim);
-  f.out = static_cast<uint16_t*>(out);
-  cudaError_t e = csa::launch_fwd(f, stream);
-  return e == cudaSuccess ? CSA_OK : cuda_fail(e);
+  return fwd_call(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity,
+                  ratio, coff, head_dim, out, stream, false);
+}
+
+csa_status_t csa_compress_fwd_exact(const void* kv, const void* score, const float* ape,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                    int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                    int32_t ratio, int32_t coff, int32_t head_dim, void* out,
+                                    cudaStream_t stream) {
+  return fwd_call(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity,
+                  ratio, coff, head_dim, out, stream, true);
 }
 
 csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ape,
@@ -139,40 +206,18 @@ csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ap
                               int32_t ratio, int32_t coff, int32_t head_dim,
                               const void* grad_out, void* dkv, void* dscore, float* dape,
                               cudaStream_t stream) {
-  csa_status_t st = validate(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
-                             capacity, ratio, coff, head_dim);
-  if (st != CSA_OK) return st;
-  if ((capacity > 0 && !grad_out) || (total_tokens > 0 && (!dkv || !dscore)) || !dape)
-    return CSA_ERR_NULL;
-  if (!aligned(grad_out, 16) || !aligned(dkv, 16) || !aligned(dscore, 16) || !aligned(dape, 16))
-    return CSA_ERR_ALIGN;
+  return bwd_call(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity,
+                  ratio, coff, head_dim, grad_out, dkv, dscore, dape, stream, false);
+}
 
-  csa::BwdParams b;
-  b.p = make_problem(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens,
-                     capacity, ratio, coff, head_dim);
-  b.grad_out = static_cast<const uint16_t*>(grad_out);
-  b.dkv = static_cast<uint16_t*>(dkv);
-  b.dscore = static_cast<uint16_t*>(dscore);
-  csa::BwdShape shape;
-  cudaError_t e = csa::plan_bwd(b.p, &shape);
-  if (e != cudaSuccess) return cuda_fail(e);
-  b.groups = shape.groups;
-
-  const int64_t n_ape = (int64_t)ratio * coff * head_dim;
-  const size_t ws_bytes = sizeof(float) * (size_t)n_ape * (size_t)shape.groups;
-  cudaMemPool_t pool;
-  e = workspace_pool(&pool);
-  if (e != cudaSuccess) return cuda_fail(e);
-  void* ws = nullptr;
-  e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream);
-  if (e != cudaSuccess) return cuda_fail(e);
-  b.partial = static_cast<float*>(ws);
-  e = csa::launch_bwd(b, shape, stream);
-  if (e == cudaSuccess) e = csa::launch_dape_reduce(b.partial, shape.groups, n_ape, dape, stream);
-  cudaError_t ef = cudaFreeAsync(ws, stream);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (ef != cudaSuccess) return cuda_fail(ef);
-  return CSA_OK;
+csa_status_t csa_compress_bwd_exact(const void* kv, const void* score, const float* ape,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                    int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                    int32_t ratio, int32_t coff, int32_t head_dim,
+                                    const void* grad_out, void* dkv, void* dscore, float* dape,
+                                    cudaStream_t stream) {
+  return bwd_call(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity,
+                  ratio, coff, head_dim, grad_out, dkv, dscore, dape, stream, true);
 }
 
 const char* csa_status_string(csa_status_t status) {

@@ -43,7 +43,7 @@ __device__ __forceinline__ void exp_cr_table(float2* tab) {
   }
 }
 
-__device__ __noinline__ float exp_cr_slow(float x) { return (float)exp((double)x); }
+static __device__ __noinline__ float exp_cr_slow(float x) { return (float)exp((double)x); }
 
 __device__ __forceinline__ float exp_cr(float x, const float2* __restrict__ tab) {
   if (!(x >= -86.0f && x <= 0.0f)) return exp_cr_slow(x);  // NaN included

@@ -47,6 +47,7 @@ struct Problem {
   int32_t d;               // head_dim
   int64_t T;               // total_tokens
   int64_t C;               // capacity
+  bool exact;              // exact mode: correctly rounded exp, IEEE division, eager order
 };
 
 struct FwdParams {

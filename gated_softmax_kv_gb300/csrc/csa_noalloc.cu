@@ -71,6 +71,7 @@ extern "C" csa_status_t csa_compress_bwd_noalloc(
   b.p.d = head_dim;
   b.p.T = total_tokens;
   b.p.C = capacity;
+  b.p.exact = false;
   b.grad_out = static_cast<const uint16_t*>(grad_out);
   b.dkv = static_cast<uint16_t*>(dkv);
   b.dscore = static_cast<uint16_t*>(dscore);

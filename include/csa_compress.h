@@ -139,6 +139,37 @@ csa_status_t csa_compress_bwd_noalloc(const void* kv, const void* score, const f
                                       const void* grad_out, void* dkv, void* dscore, float* dape,
                                       cudaStream_t stream);
 
+/*
+ * Exact mode (cuDNN-frontend "CSA Fused Compressor", section "Numerics":
+ * bitwise agreement with an fp32 eager reference is the aim for ratios 2 and
+ * 4). Same arguments, layouts, outputs and ownership as csa_compress_fwd /
+ * csa_compress_bwd; what changes is the arithmetic of the softmax weights:
+ * exp is correctly rounded (the exact value rounded once to fp32), p_k =
+ * e_k / den with IEEE division, and the forward sums p_k * kv_k with each
+ * product and sum rounded separately, in slot order. With it, out, dkv and
+ * dscore are the bits of an fp32 reference that takes those steps in that
+ * order (max, exp, den, p, then the pooled sum or the backward's S); dape
+ * is reduced as in csa_compress_bwd, so it is deterministic but not bitwise
+ * equal to a reference that sums in another order.
+ *
+ * Supported only for windows of at most 8 slots (coff * ratio <= 8: ratio
+ * 2, 4 or 8 with coff 1, ratio 2 or 4 with coff 2); other shapes return
+ * CSA_ERR_UNSUPPORTED and launch nothing. It is slower than the default
+ * mode, whose fast exp leaves a small fraction of outputs one bf16 step from
+ * the eager reference.
+ */
+csa_status_t csa_compress_fwd_exact(const void* kv, const void* score, const float* ape,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                    int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                    int32_t ratio, int32_t coff, int32_t head_dim,
+                                    void* out, cudaStream_t stream);
+csa_status_t csa_compress_bwd_exact(const void* kv, const void* score, const float* ape,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                    int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                    int32_t ratio, int32_t coff, int32_t head_dim,
+                                    const void* grad_out, void* dkv, void* dscore, float* dape,
+                                    cudaStream_t stream);
+
 /* Static description of a status code (never null). */
 const char* csa_status_string(csa_status_t status);
 

@@ -62,16 +62,16 @@ class DeviceCase:
         self.cuc = torch.from_numpy(case.cu_seqlens_comp.astype(np.int32)).cuda()
         self.grad_out = dev_bf16(case.grad_out)
 
-    def fwd(self, prefill: int = 0x7FC0):
+    def fwd(self, prefill: int = 0x7FC0, exact: bool = False):
         c = self.case
         out = Guarded((c.capacity, c.head_dim), "bf16", prefill)
         gsk.csa_compress_fwd(self.kv, self.score, self.ape, self.cu, self.cuc, c.capacity, c.ratio,
-                             c.coff, c.head_dim, out=out.inner)
+                             c.coff, c.head_dim, out=out.inner, exact=exact)
         torch_mod().cuda.synchronize()
         assert out.guards_intact(), "forward wrote outside out"
         return host_bits(out.inner)
 
-    def bwd(self, prefill: int = 0x7FC0, grad_out=None):
+    def bwd(self, prefill: int = 0x7FC0, grad_out=None, exact: bool = False):
         torch = torch_mod()
         c = self.case
         dkv = Guarded(self.kv.shape, "bf16", prefill)
@@ -79,7 +79,8 @@ class DeviceCase:
         dape = Guarded(self.ape.shape, "f32", 0x7FC00000 if prefill == 0x7FC0 else prefill << 16)
         go = self.grad_out if grad_out is None else grad_out
         gsk.csa_compress_bwd(self.kv, self.score, self.ape, self.cu, self.cuc, c.capacity, c.ratio,
-                             c.coff, c.head_dim, go, dkv=dkv.inner, dscore=ds.inner, dape=dape.inner)
+                             c.coff, c.head_dim, go, dkv=dkv.inner, dscore=ds.inner, dape=dape.inner,
+                             exact=exact)
         torch.cuda.synchronize()
         assert dkv.guards_intact() and ds.guards_intact() and dape.guards_intact(), \
             "backward wrote outside its outputs"

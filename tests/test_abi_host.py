@@ -55,24 +55,34 @@ def test_status_strings(lib):
 A = 0x10000
 
 
-def fwd(lib, **kw):
+def fwd(lib, exact=False, **kw):
     args = dict(kv=A, score=A, ape=A, cu=A, cuc=A, nseq=1, T=64, C=8, r=4, coff=2, d=64, out=A)
     args.update(kw)
-    return lib.csa_compress_fwd(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
+    fn = lib.csa_compress_fwd_exact if exact else lib.csa_compress_fwd
+    return fn(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
                                 args["nseq"], args["T"], args["C"], args["r"], args["coff"],
                                 args["d"], args["out"], None)
 
 
-def bwd(lib, **kw):
+def bwd(lib, exact=False, **kw):
     args = dict(kv=A, score=A, ape=A, cu=A, cuc=A, nseq=1, T=64, C=8, r=4, coff=2, d=64, go=A,
                 dkv=A, ds=A, dape=A)
     args.update(kw)
-    return lib.csa_compress_bwd(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
+    fn = lib.csa_compress_bwd_exact if exact else lib.csa_compress_bwd
+    return fn(args["kv"], args["score"], args["ape"], args["cu"], args["cuc"],
                                 args["nseq"], args["T"], args["C"], args["r"], args["coff"],
                                 args["d"], args["go"], args["dkv"], args["ds"], args["dape"], None)
 
 
-@pytest.mark.parametrize("call", [fwd, bwd])
+def fwd_exact(lib, **kw):
+    return fwd(lib, exact=True, **kw)
+
+
+def bwd_exact(lib, **kw):
+    return bwd(lib, exact=True, **kw)
+
+
+@pytest.mark.parametrize("call", [fwd, bwd, fwd_exact, bwd_exact])
 def test_validation_rejects_before_launch(lib, call):
     assert call(lib, r=3) == 3                  # unsupported ratio
     assert call(lib, r=256) == 3
@@ -105,6 +115,20 @@ def test_bwd_output_pointers_validated(lib):
 def test_fwd_zero_capacity_launches_nothing(lib):
     # capacity == 0: valid, no launch, no CUDA call (works without a GPU)
     assert fwd(lib, C=0, out=0) == 0
+    assert fwd(lib, exact=True, C=0, out=0) == 0
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_exact_mode_envelope(lib, exact):
+    # the exact mode covers windows of at most 8 slots; wider ones are
+    # rejected before any CUDA call (zero capacity: nothing would launch)
+    for r, coff in [(2, 1), (4, 1), (8, 1), (2, 2), (4, 2)]:
+        assert fwd(lib, exact=exact, r=r, coff=coff, C=0, out=0) == 0
+    for r, coff in [(8, 2), (16, 1), (16, 2), (128, 1), (128, 2)]:
+        want = 3 if exact else 0
+        assert fwd(lib, exact=exact, r=r, coff=coff, C=0, out=0) == want
+        # the shape is checked before the output pointers
+        assert bwd(lib, exact=exact, r=r, coff=coff, T=256, d=64, go=0) == (3 if exact else 1)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
