@@ -28,7 +28,6 @@
 
 #include "csa_bwd_common.cuh"
 #include "csa_device.cuh"
-#include "csa_exp_cr.cuh"
 #include "csa_internal.h"
 
 namespace csa {
@@ -55,10 +54,8 @@ constexpr int kCv = 4;  // columns per thread (8-byte vectors)
 // Small window (W <= 8): blockDim = (TX, TY); a thread owns 4 consecutive
 // columns (8-byte vectors) of one row at a time, rows strided by the grid.
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
-// D == 0 reads it from the problem. EXACT selects the exact mode
-// (csa_compress_bwd_exact): the correctly rounded exp and p = e / den with
-// IEEE division, the rest of the order unchanged.
-template <int R, int COFF, int D, bool EXACT>
+// D == 0 reads it from the problem.
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_small_kernel(const BwdParams bp) {
   grid_dependency_wait();
@@ -79,8 +76,6 @@ bwd_small_kernel(const BwdParams bp) {
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
-  __shared__ float2 exp_tab[EXACT ? kExpTableSize : 1];
-  if (EXACT) exp_cr_table(exp_tab);  // ready after the barrier below
   // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
@@ -146,15 +141,10 @@ bwd_small_kernel(const BwdParams bp) {
           float den = 0.0f;
 #pragma unroll
           for (int k = 0; k < W; ++k) {
-            pz[k][c] = EXACT ? exp_cr(__fsub_rn(pz[k][c], m), exp_tab)
-                             : CSA_BWD_SMALL_EXP(__fsub_rn(pz[k][c], m));
+            pz[k][c] = CSA_BWD_SMALL_EXP(__fsub_rn(pz[k][c], m));
             den = __fadd_rn(den, pz[k][c]);
           }
           const float y = __frcp_rn(den);
-          if (EXACT) {
-#pragma unroll
-            for (int k = 0; k < W; ++k) pz[k][c] = __fdiv_rn(pz[k][c], den);
-          } else {
 #if CSA_BWD_SMALL_DIV_RN
 #pragma unroll
           for (int k = 0; k < W; ++k) pz[k][c] = div_rn_by_rcp(pz[k][c], den, y);
@@ -162,7 +152,6 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
           for (int k = 0; k < W; ++k) pz[k][c] = __fmul_rn(pz[k][c], y);
 #endif
-          }
           g[h] = bf16_at(c2 ? gv.y : gv.x, h);
           float acc = 0.0f;
 #pragma unroll
@@ -307,7 +296,7 @@ dape_reduce_kernel(const float4* __restrict__ partial, int32_t groups, int64_t n
   if (threadIdx.y == 0 && e < n4) dape[e] = *mine;
 }
 
-template <int R, int COFF, int D, bool EXACT>
+template <int R, int COFF, int D>
 cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   constexpr int W = COFF * R;
   const int ncv = p.d / kCv;
@@ -315,7 +304,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (ncv + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kCv;
-  auto kern = bwd_small_kernel<R, COFF, D, EXACT>;
+  auto kern = bwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
   int64_t gy = (int64_t)sm_count() * occ / tiles;
@@ -330,30 +319,18 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   return cudaSuccess;
 }
 
-template <int R, int COFF, bool EXACT>
-cudaError_t plan_small_x(const Problem& p, BwdShape* s) {
-  if (p.d == 512) return plan_small_d<R, COFF, 512, EXACT>(p, s);
-  if (p.d == 128) return plan_small_d<R, COFF, 128, EXACT>(p, s);
-  return plan_small_d<R, COFF, 0, EXACT>(p, s);
-}
-
 template <int R, int COFF>
 cudaError_t plan_small(const Problem& p, BwdShape* s) {
-  return p.exact ? plan_small_x<R, COFF, true>(p, s) : plan_small_x<R, COFF, false>(p, s);
-}
-
-template <int R, int COFF, bool EXACT>
-cudaError_t run_small_x(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  auto kern = b.p.d == 512 ? bwd_small_kernel<R, COFF, 512, EXACT>
-             : b.p.d == 128 ? bwd_small_kernel<R, COFF, 128, EXACT>
-                            : bwd_small_kernel<R, COFF, 0, EXACT>;
-  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
+  if (p.d == 512) return plan_small_d<R, COFF, 512>(p, s);
+  if (p.d == 128) return plan_small_d<R, COFF, 128>(p, s);
+  return plan_small_d<R, COFF, 0>(p, s);
 }
 
 template <int R, int COFF>
 cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  return b.p.exact ? run_small_x<R, COFF, true>(b, s, stream)
-                   : run_small_x<R, COFF, false>(b, s, stream);
+  auto kern = b.p.d == 512 ? bwd_small_kernel<R, COFF, 512>
+             : b.p.d == 128 ? bwd_small_kernel<R, COFF, 128> : bwd_small_kernel<R, COFF, 0>;
+  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
 }
 
 #define CSA_BWD_SMALL_DISPATCH(FN, ...)                       \
@@ -369,12 +346,14 @@ cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream
 }  // namespace
 
 cudaError_t plan_bwd(const Problem& p, BwdShape* shape) {
+  if (p.exact) return plan_bwd_exact(p, shape);
   CSA_BWD_SMALL_DISPATCH(plan_small, p, shape)
   return plan_bwd_long(p, shape);  // windows of 16 slots and more
 }
 
 cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
   const Problem& p = b.p;
+  if (p.exact) return launch_bwd_exact(b, shape, stream);
   CSA_BWD_SMALL_DISPATCH(run_small, b, shape, stream)
   return launch_bwd_long(b, shape, stream);
 }

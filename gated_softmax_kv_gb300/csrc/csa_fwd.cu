@@ -37,7 +37,6 @@
 #include <utility>
 
 #include "csa_device.cuh"
-#include "csa_exp_cr.cuh"
 #include "csa_internal.h"
 
 namespace csa {
@@ -57,10 +56,7 @@ constexpr int kThreads = 256;
 
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
 // D == 0 reads it from the problem.
-// EXACT: the exact mode (csa_compress_fwd_exact): the correctly rounded exp
-// and the eager order of the fp32 reference, p_k = e_k / den (IEEE division)
-// then out = sum_k p_k kv_k with every product and sum rounded separately.
-template <int R, int COFF, int D, bool EXACT>
+template <int R, int COFF, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 fwd_small_kernel(const FwdParams f) {
   grid_dependency_wait();
@@ -80,8 +76,6 @@ fwd_small_kernel(const FwdParams f) {
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
-  __shared__ float2 exp_tab[EXACT ? kExpTableSize : 1];
-  if (EXACT) exp_cr_table(exp_tab);  // ready after the barrier below
   // APE slice of this column tile, [W][tile_cols], read once per CTA
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
@@ -131,34 +125,6 @@ fwd_small_kernel(const FwdParams f) {
     }
     // m = max z, e = exp(z - m), den = sum e, out = (sum e * kv) / den
     uint32_t ow[4];
-    if (EXACT) {
-#pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2) {
-        float res[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float m = h ? z[0][c2].y : z[0][c2].x;
-#pragma unroll
-          for (int k = 1; k < W; ++k) m = max_nan(m, h ? z[k][c2].y : z[k][c2].x);
-          float e[W], den = 0.0f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            e[k] = exp_cr(__fsub_rn(h ? z[k][c2].y : z[k][c2].x, m), exp_tab);
-            den = __fadd_rn(den, e[k]);
-          }
-          float acc = 0.0f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const uint32_t kw = c2 == 0 ? kvv[k].x : c2 == 1 ? kvv[k].y : c2 == 2 ? kvv[k].z : kvv[k].w;
-            acc = __fadd_rn(acc, __fmul_rn(__fdiv_rn(e[k], den), bf16_at(kw, h)));
-          }
-          res[h] = acc;
-        }
-        ow[c2] = pack_bf16x2(res[0], res[1]);
-      }
-      st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
-      continue;
-    }
 #pragma unroll
     for (int c2 = 0; c2 < 4; ++c2) {
       float m0 = z[0][c2].x, m1 = z[0][c2].y;
@@ -182,7 +148,7 @@ fwd_small_kernel(const FwdParams f) {
   }
 }
 
-template <int R, int COFF, int D, bool EXACT>
+template <int R, int COFF, int D>
 cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   constexpr int W = COFF * R;
   const int nvec = f.p.d / kVec;
@@ -190,7 +156,7 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (nvec + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kVec;
-  auto kern = fwd_small_kernel<R, COFF, D, EXACT>;
+  auto kern = fwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
   const int64_t row_blocks = (f.p.C + ty - 1) / ty;
@@ -201,17 +167,11 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream, f);
 }
 
-template <int R, int COFF, bool EXACT>
-cudaError_t launch_small_x(const FwdParams& f, cudaStream_t stream) {
-  if (f.p.d == 512) return launch_small_d<R, COFF, 512, EXACT>(f, stream);
-  if (f.p.d == 128) return launch_small_d<R, COFF, 128, EXACT>(f, stream);
-  return launch_small_d<R, COFF, 0, EXACT>(f, stream);
-}
-
 template <int R, int COFF>
 cudaError_t launch_small(const FwdParams& f, cudaStream_t stream) {
-  return f.p.exact ? launch_small_x<R, COFF, true>(f, stream)
-                   : launch_small_x<R, COFF, false>(f, stream);
+  if (f.p.d == 512) return launch_small_d<R, COFF, 512>(f, stream);
+  if (f.p.d == 128) return launch_small_d<R, COFF, 128>(f, stream);
+  return launch_small_d<R, COFF, 0>(f, stream);
 }
 
 }  // namespace
@@ -226,6 +186,7 @@ bool supported(int ratio, int coff) {
 
 cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
   if (f.p.C == 0) return cudaSuccess;
+  if (f.p.exact) return launch_fwd_exact(f, stream);
   switch (f.p.ratio * 4 + f.p.coff) {
     case 2 * 4 + 1: return launch_small<2, 1>(f, stream);
     case 2 * 4 + 2: return launch_small<2, 2>(f, stream);

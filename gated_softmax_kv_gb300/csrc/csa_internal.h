@@ -1,6 +1,6 @@
 // Internal interface between the C ABI (csa_api.cu, csa_noalloc.cu) and the
 // kernel translation units (csa_fwd.cu, csa_fwd_long.cu, csa_bwd.cu,
-// csa_bwd_long.cu). Not installed, not part of the ABI.
+// csa_bwd_long.cu, csa_exact.cu). Not installed, not part of the ABI.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -82,6 +82,10 @@ cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t s
 cudaError_t launch_fwd_long(const FwdParams& f, cudaStream_t stream);
 cudaError_t plan_bwd_long(const Problem& p, BwdShape* shape);
 cudaError_t launch_bwd_long(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
+// The exact mode, windows of at most 8 slots (csa_exact.cu).
+cudaError_t launch_fwd_exact(const FwdParams& f, cudaStream_t stream);
+cudaError_t plan_bwd_exact(const Problem& p, BwdShape* shape);
+cudaError_t launch_bwd_exact(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
                                cudaStream_t stream);
 

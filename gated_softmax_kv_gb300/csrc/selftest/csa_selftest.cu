@@ -30,7 +30,8 @@ __global__ void div_kernel(const float* __restrict__ a, const float* __restrict_
 
 // The two-lane fp32 helpers one operation at a time (every result stored, so
 // nothing can be fused), in the chains the kernels use (a product feeding a
-// product, a difference feeding a product, an FMA), and the scalar FMA.
+// product, a difference feeding a product, an FMA, a scalar product feeding
+// a two-lane sum or difference), and the scalar FMA.
 __global__ void pair_ops_kernel(const float2* __restrict__ a, const float2* __restrict__ b,
                                 const float2* __restrict__ c, float2* __restrict__ out,
                                 int64_t n) {
@@ -44,25 +45,53 @@ __global__ void pair_ops_kernel(const float2* __restrict__ a, const float2* __re
     out[4 * n + i] = csa::mul2_rn(csa::sub2_rn(x, y), z);
     out[5 * n + i] = csa::fma2_rn(x, y, z);
     out[6 * n + i] = make_float2(__fmaf_rn(x.x, y.x, z.x), __fmaf_rn(x.y, y.y, z.y));
+    // scalar products feeding two-lane sums, as the exact mode chains them
+    out[7 * n + i] = csa::add2_rn(x, make_float2(__fmul_rn(y.x, z.x), __fmul_rn(y.y, z.y)));
+    out[8 * n + i] = csa::sub2_rn(make_float2(__fmul_rn(x.x, y.x), __fmul_rn(x.y, y.y)), z);
   }
 }
 
-__global__ void exp_cr_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
-  __shared__ float2 tab[csa::kExpTableSize];
+__global__ void exp_cr2_kernel(const float2* __restrict__ x, float2* __restrict__ y, int64_t n) {
+  __shared__ float tab[2 * csa::kExpTableSize];
   csa::exp_cr_table(tab);
   __syncthreads();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = csa::exp_cr(x[i], tab);
+    y[i] = csa::exp_cr2(x[i], tab);
+}
+
+__global__ void div2_kernel(const float2* __restrict__ a, const float2* __restrict__ b,
+                            float2* __restrict__ q, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float2 bb = b[i];
+    q[i] = csa::div2_cr(a[i], bb, make_float2(-bb.x, -bb.y),
+                        make_float2(__frcp_rn(bb.x), __frcp_rn(bb.y)));
+  }
 }
 
 }  // namespace
 
-extern "C" int32_t csa_selftest_exp_cr(const float* x, float* y, int64_t n, cudaStream_t stream) {
-  if (n <= 0) return 0;
-  int64_t blocks = (n + 255) / 256;
+// div2_cr on n_pairs operand pairs (a[2i], a[2i + 1]) / (b[2i], b[2i + 1]).
+extern "C" int32_t csa_selftest_div2(const float* a, const float* b, float* q, int64_t n_pairs,
+                                     cudaStream_t stream) {
+  if (n_pairs <= 0) return 0;
+  int64_t blocks = (n_pairs + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  exp_cr_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, n);
+  div2_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float2*>(a),
+                                                    reinterpret_cast<const float2*>(b),
+                                                    reinterpret_cast<float2*>(q), n_pairs);
+  return (int32_t)cudaGetLastError();
+}
+
+// exp_cr2 on n_pairs argument pairs (x[2i], x[2i + 1]).
+extern "C" int32_t csa_selftest_exp_cr2(const float* x, float* y, int64_t n_pairs,
+                                        cudaStream_t stream) {
+  if (n_pairs <= 0) return 0;
+  int64_t blocks = (n_pairs + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  exp_cr2_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float2*>(x),
+                                                       reinterpret_cast<float2*>(y), n_pairs);
   return (int32_t)cudaGetLastError();
 }
 

@@ -127,8 +127,9 @@ def test_forward_fast_exp_error_bound():
 def test_two_lane_fp32_ops_round_like_scalar():
     """The f32x2 helpers of the kernels (add/sub/mul/fma .rn.f32x2) against
     numpy's fp32 arithmetic, one rounding per operation: each alone, a product
-    feeding a product, a difference feeding a product, and the two-lane FMA
-    against the scalar FMA. (A product feeding an add or a subtract may be
+    feeding a product, a difference feeding a product, a scalar product
+    feeding a two-lane sum or difference, and the two-lane FMA against the
+    scalar FMA. (A two-lane product feeding a two-lane add or subtract may be
     fused by the compiler; the kernels never chain them that way.) Random
     operands over wide exponent ranges plus signed zeros, infinities, NaN and
     subnormals."""
@@ -149,13 +150,15 @@ def test_two_lane_fp32_ops_round_like_scalar():
     special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-40, -3e-39, 3.4e38], np.float32)
     a[:8], b[8:16], c[16:24] = special, special, special
     dev = [torch.from_numpy(x).cuda() for x in (a, b, c)]
-    out = torch.empty(7 * n, dtype=torch.float32, device="cuda")
+    out = torch.empty(9 * n, dtype=torch.float32, device="cuda")
     assert lib.csa_selftest_pair_ops(*(t.data_ptr() for t in dev), out.data_ptr(), n // 2, None) == 0
     torch.cuda.synchronize()
-    got = out.cpu().numpy().reshape(7, n)
+    got = out.cpu().numpy().reshape(9, n)
     with np.errstate(all="ignore"):
-        want = [a + b, a - c, b * c, (a * b) * c, (a - b) * c]  # numpy fp32: one rounding per step
-    for row, w in enumerate(want):
+        # numpy fp32: one rounding per step
+        want = {0: a + b, 1: a - c, 2: b * c, 3: (a * b) * c, 4: (a - b) * c, 7: a + b * c,
+                8: a * b - c}
+    for row, w in want.items():
         same = (got[row].view(np.uint32) == w.view(np.uint32)) | (np.isnan(got[row]) & np.isnan(w))
         assert same.all(), f"pattern {row}: {int((~same).sum())} differ"
     same = (got[5].view(np.uint32) == got[6].view(np.uint32)) | (np.isnan(got[5]) & np.isnan(got[6]))
@@ -163,28 +166,31 @@ def test_two_lane_fp32_ops_round_like_scalar():
 
 
 def test_correctly_rounded_exp_matches_the_oracle():
-    """exp_cr (the exact mode's exp) against the oracle's exp (fp64 exp rounded
-    once to fp32), bit for bit: every 61st fp32 value in [-86, 0] (the
-    table-driven path and its rounding test), a dense sweep of [-1, 0],
-    [-104, -86] (the fp64 path, down through the subnormals to 0) and the
-    special values."""
+    """exp_cr2 (the exact mode's exp, two arguments per call) against the
+    oracle's exp (fp64 exp rounded once to fp32), bit for bit: every 61st
+    fp32 value in [-86, 0] (the table-driven path and its rounding test), a
+    dense sweep of [-1, 0], [-104, -86] (the fp64 path, down through the
+    subnormals to 0), the special values, and a shuffled copy of all of it so
+    that pairs mix the two paths."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from gated_softmax_kv_gb300 import nvbuild
     nvbuild.build()
     lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
-    lib.csa_selftest_exp_cr.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                                        ctypes.c_void_p]
-    lib.csa_selftest_exp_cr.restype = ctypes.c_int32
+    fn = lib.csa_selftest_exp_cr2
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
     lo, hi = np.float32(-86.0).view(np.uint32), np.uint32(0x80000000)
     xs = np.concatenate([
         np.arange(hi, lo, 61, dtype=np.uint64).astype(np.uint32).view(np.float32),
         np.linspace(-1.0, 0.0, 1 << 22, dtype=np.float32),
         np.linspace(-104.0, -86.0, 1 << 20, dtype=np.float32),
-        np.array([0.0, -0.0, -np.inf, np.nan, -86.0, -87.0, -103.97, -1e-30], np.float32)])
+        np.array([0.0, -0.0, -np.inf, np.nan, -86.0, -87.0, -103.97, -103.98, -104.0, -1e-30,
+                  np.inf, 1.0], np.float32)])
+    xs = np.concatenate([xs, np.random.default_rng(3).permutation(xs)])
     x_d = torch.from_numpy(xs).cuda()
     y_d = torch.empty_like(x_d)
-    assert lib.csa_selftest_exp_cr(x_d.data_ptr(), y_d.data_ptr(), xs.size, None) == 0
+    assert fn(x_d.data_ptr(), y_d.data_ptr(), xs.size // 2, None) == 0
     torch.cuda.synchronize()
     got = y_d.cpu().numpy()
     want = oracle.exp_f32_array(xs)
@@ -192,3 +198,38 @@ def test_correctly_rounded_exp_matches_the_oracle():
     bad = np.nonzero(~same)[0]
     detail = [(float(xs[i]), float(got[i]), float(want[i])) for i in bad[:8]]
     assert bad.size == 0, f"{bad.size} of {xs.size} differ (x, got, want): {detail}"
+
+
+def test_exact_mode_division_is_ieee():
+    """div2_cr, the exact mode's e / den (one reciprocal per column, the
+    correction step, IEEE division below 2^-102), against IEEE fp32 division
+    on the softmax domain e in [0, 1], den in [1, 8], with e spread down to
+    2^-149 and exact zeros, and with NaN denominators; every result, subnormal
+    quotients included, must carry IEEE's bits."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    fn = lib.csa_selftest_div2
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
+    rng = np.random.default_rng(11)
+    n = 1 << 23
+    a = np.concatenate([rng.random(n, dtype=np.float32),
+                        (2.0 ** rng.uniform(-149, 0, n)).astype(np.float32),
+                        np.zeros(64, np.float32), np.ones(64, np.float32)])
+    b = np.concatenate([rng.uniform(1.0, 8.0, n).astype(np.float32),
+                        rng.uniform(1.0, 8.0, n).astype(np.float32),
+                        rng.uniform(1.0, 8.0, 64).astype(np.float32),
+                        np.full(64, np.nan, np.float32)])
+    a_d, b_d = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    q_d = torch.empty_like(a_d)
+    assert fn(a_d.data_ptr(), b_d.data_ptr(), q_d.data_ptr(), a.size // 2, None) == 0
+    torch.cuda.synchronize()
+    got = q_d.cpu().numpy()
+    want = a / b
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    bad = np.nonzero(~same)[0]
+    detail = [(float(a[i]), float(b[i]), float(got[i]), float(want[i])) for i in bad[:8]]
+    assert bad.size == 0, f"{bad.size} quotients differ (a, b, got, want): {detail}"
