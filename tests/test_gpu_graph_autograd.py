@@ -37,8 +37,8 @@ def _bits(t):
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "r128c1"])
-def test_graph_replay_matches_eager(gsk, name):
+@pytest.mark.parametrize("name,exact", [("tiny", False), ("r128c1", False), ("r4d512", True)])
+def test_graph_replay_matches_eager(gsk, name, exact):
     case = workloads.config(name)
     t = _up(case)
     args = (case.capacity, case.ratio, case.coff, case.head_dim)
@@ -46,9 +46,10 @@ def test_graph_replay_matches_eager(gsk, name):
     dkv, ds, dape = torch.empty_like(t["kv"]), torch.empty_like(t["score"]), torch.empty_like(t["ape"])
 
     def step():
-        gsk.csa_compress_fwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], *args, out=out)
+        gsk.csa_compress_fwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], *args, out=out,
+                             exact=exact)
         gsk.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], *args, t["go"],
-                             dkv=dkv, dscore=ds, dape=dape)
+                             dkv=dkv, dscore=ds, dape=dape, exact=exact)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -82,7 +83,8 @@ def test_graph_replay_matches_eager(gsk, name):
         assert np.array_equal(a, b)
 
 
-def test_autograd_wrapper_matches_the_c_abi(gsk):
+@pytest.mark.parametrize("exact", [False, True])
+def test_autograd_wrapper_matches_the_c_abi(gsk, exact):
     from gated_softmax_kv_gb300.autograd import compressor
     case = workloads.config("tiny")
     t = _up(case)
@@ -90,13 +92,13 @@ def test_autograd_wrapper_matches_the_c_abi(gsk):
     score = t["score"].clone().requires_grad_(True)
     ape = t["ape"].clone().requires_grad_(True)
     out = compressor(kv, score, ape, t["cu"], t["cuc"], case.ratio, case.coff, case.head_dim,
-                     capacity=case.capacity)
+                     capacity=case.capacity, exact=exact)
     out.backward(t["go"])
     ref_out = gsk.csa_compress_fwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], case.capacity,
-                                   case.ratio, case.coff, case.head_dim)
+                                   case.ratio, case.coff, case.head_dim, exact=exact)
     r_dkv, r_ds, r_dape = gsk.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
                                                case.capacity, case.ratio, case.coff, case.head_dim,
-                                               t["go"])
+                                               t["go"], exact=exact)
     torch.cuda.synchronize()
     assert np.array_equal(_bits(out.detach()), _bits(ref_out))
     assert np.array_equal(_bits(kv.grad), _bits(r_dkv))
