@@ -54,6 +54,48 @@ constexpr int kThreads = 256;
 #define CSA_FWD_EXP2(x) softmax_exp_fast2(x)
 #endif
 
+// One output row's 8 columns from the window's kv / score vectors (masked
+// slots already kv = 0, score = -inf) and the APE slice: logits z = score +
+// ape, m = max z, e = exp(z - m), den = sum e in slot order, out = (sum e kv)
+// / den, one bf16 rounding. The columns go in pairs through the two-lane fp32
+// instructions (each lane rounded as the scalar operation).
+template <int W>
+__device__ __forceinline__ uint4 small_row_out(const uint4 (&kvv)[W], const uint4 (&scv)[W],
+                                               const float* ape_s, int tile_cols) {
+  float2 z[W][kVec / 2];
+#pragma unroll
+  for (int k = 0; k < W; ++k) {
+    const float4 a0 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
+    const float4 a1 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols + 4);
+    z[k][0] = add2_rn(make_float2(bf16_lo(scv[k].x), bf16_hi(scv[k].x)), make_float2(a0.x, a0.y));
+    z[k][1] = add2_rn(make_float2(bf16_lo(scv[k].y), bf16_hi(scv[k].y)), make_float2(a0.z, a0.w));
+    z[k][2] = add2_rn(make_float2(bf16_lo(scv[k].z), bf16_hi(scv[k].z)), make_float2(a1.x, a1.y));
+    z[k][3] = add2_rn(make_float2(bf16_lo(scv[k].w), bf16_hi(scv[k].w)), make_float2(a1.z, a1.w));
+  }
+  // m = max z, e = exp(z - m), den = sum e, out = (sum e * kv) / den
+  uint32_t ow[4];
+#pragma unroll
+  for (int c2 = 0; c2 < 4; ++c2) {
+    float m0 = z[0][c2].x, m1 = z[0][c2].y;
+#pragma unroll
+    for (int k = 1; k < W; ++k) {
+      m0 = max_nan(m0, z[k][c2].x);
+      m1 = max_nan(m1, z[k][c2].y);
+    }
+    const float2 m = make_float2(m0, m1);
+    float2 den = make_float2(0.0f, 0.0f), acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const float2 e = CSA_FWD_EXP2(sub2_rn(z[k][c2], m));
+      den = add2_rn(den, e);
+      const uint32_t kw = c2 == 0 ? kvv[k].x : c2 == 1 ? kvv[k].y : c2 == 2 ? kvv[k].z : kvv[k].w;
+      acc = fma2_rn(e, make_float2(bf16_lo(kw), bf16_hi(kw)), acc);
+    }
+    ow[c2] = pack_bf16x2(__fdiv_rn(acc.x, den.x), __fdiv_rn(acc.y, den.y));
+  }
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
 // D == 0 reads it from the problem.
 template <int R, int COFF, int D>
@@ -111,40 +153,7 @@ fwd_small_kernel(const FwdParams f) {
         scv[k] = ld_stream(sc_row + koff(k));
       }
     }
-    // logits z = score + ape; columns in pairs through the two-lane fp32
-    // instructions (each lane rounded as the scalar operation)
-    float2 z[W][kVec / 2];
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
-      const float4 a1 = *reinterpret_cast<const float4*>(ape_s + k * tile_cols + 4);
-      z[k][0] = add2_rn(make_float2(bf16_lo(scv[k].x), bf16_hi(scv[k].x)), make_float2(a0.x, a0.y));
-      z[k][1] = add2_rn(make_float2(bf16_lo(scv[k].y), bf16_hi(scv[k].y)), make_float2(a0.z, a0.w));
-      z[k][2] = add2_rn(make_float2(bf16_lo(scv[k].z), bf16_hi(scv[k].z)), make_float2(a1.x, a1.y));
-      z[k][3] = add2_rn(make_float2(bf16_lo(scv[k].w), bf16_hi(scv[k].w)), make_float2(a1.z, a1.w));
-    }
-    // m = max z, e = exp(z - m), den = sum e, out = (sum e * kv) / den
-    uint32_t ow[4];
-#pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2) {
-      float m0 = z[0][c2].x, m1 = z[0][c2].y;
-#pragma unroll
-      for (int k = 1; k < W; ++k) {
-        m0 = max_nan(m0, z[k][c2].x);
-        m1 = max_nan(m1, z[k][c2].y);
-      }
-      const float2 m = make_float2(m0, m1);
-      float2 den = make_float2(0.0f, 0.0f), acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const float2 e = CSA_FWD_EXP2(sub2_rn(z[k][c2], m));
-        den = add2_rn(den, e);
-        const uint32_t kw = c2 == 0 ? kvv[k].x : c2 == 1 ? kvv[k].y : c2 == 2 ? kvv[k].z : kvv[k].w;
-        acc = fma2_rn(e, make_float2(bf16_lo(kw), bf16_hi(kw)), acc);
-      }
-      ow[c2] = pack_bf16x2(__fdiv_rn(acc.x, den.x), __fdiv_rn(acc.y, den.y));
-    }
-    st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+    st_stream(dst, small_row_out<W>(kvv, scv, ape_s, tile_cols));
   }
 }
 

@@ -195,9 +195,13 @@ fwd_long_kernel(const FwdParams f, const int split) {
 // Warps per row of the long-window forward: the smallest power of two (up to
 // kLongRows and to the batches in a window) that gives at least
 // CSA_FWD_SPLIT_WARPS warps over the whole problem. It depends on the problem
-// only, never on the device, so results are the same on every GPU.
+// only, never on the device, so results are the same on every GPU. 2048
+// measured best: against 4096 it keeps one warp per row where that already
+// gives 2048 warps (65536-token, head_dim 512 packs) and halves the split of
+// the head_dim 128 ratio-128 packs (19.8 instead of 22.3 us at 131072 tokens,
+// 21.0 instead of 22.9 us at 65536 with coff 2); 1024 loses at coff 2.
 #ifndef CSA_FWD_SPLIT_WARPS
-#define CSA_FWD_SPLIT_WARPS 4096
+#define CSA_FWD_SPLIT_WARPS 2048
 #endif
 
 template <int R, int COFF>
