@@ -23,11 +23,11 @@
 //     floats, the cubic tail in fp32 (below 2^-25), as a two-float sum.
 //   * 2^(j/64) = T_hi + T_lo from a 64-entry table built per CTA in fp64.
 //   * y + er = T (1 + (e^r - 1)) with error below 2^-46 relative; y is the
-//     correctly rounded result when y + er - 2^-42 y and y + er + 2^-42 y
-//     both round to y (Ziv's test), which fails for about one argument in
-//     2^17; those arguments go to fp64 exp rounded once, as do NaN and
-//     |x| > 86. Arguments <= -104 (e^x < 2^-150, half the smallest
-//     subnormal) give +0.
+//     correctly rounded result when y + er (1 + 2^-16) rounds to y (a
+//     rounding test with a 16-fold margin on that bound), which fails for
+//     about one argument in 2^16; those arguments go to fp64 exp rounded
+//     once, as do NaN and |x| > 86. Arguments <= -104 (e^x < 2^-150, half
+//     the smallest subnormal) give +0.
 //   * The result is y 2^k (exact: y 2^k is normal for k >= -125).
 #pragma once
 
@@ -117,17 +117,21 @@ __device__ __forceinline__ float2 exp_cr2(float2 x, const float* __restrict__ ta
   const float2 tt = add2_rn(e2, b);
   const float2 y = add2_rn(s2, tt);  // Fast2Sum(s2, tt)
   const float2 er = sub2_rn(tt, sub2_rn(y, s2));
-  // 2^k: the exponent field of (t's encoding << 17) is k mod 256
-  const float2 res = mul2_rn(
-      y, make_float2(__int_as_float(((b0 << 17) + 0x3f800000) & 0x7f800000),
-                     __int_as_float(((b1 << 17) + 0x3f800000) & 0x7f800000)));
-  // rounding test: the exact value lies strictly between y + er - m and
-  // y + er + m, m = 2^-42 y (exact); rounding is monotonic, so if both ends
-  // round to y, so does the exact value (y = RN(y + er) in any case)
-  const float2 m = mul2_rn(y, make_float2(__int_as_float(0x2a800000), __int_as_float(0x2a800000)));
-  const float2 hi = add2_rn(y, add2_rn(er, m)), lo = add2_rn(y, sub2_rn(er, m));
-  const bool ok0 = in0 && hi.x == y.x && lo.x == y.x;
-  const bool ok1 = in1 && hi.y == y.y && lo.y == y.y;
+  // y 2^k: k << 23 is (t's encoding << 17) with the low 23 bits cleared (the
+  // index bits move there); added to y's encoding it scales y exactly, since
+  // the result stays normal
+  const float2 res =
+      make_float2(__uint_as_float(__float_as_uint(y.x) + (((uint32_t)b0 << 17) & 0xff800000u)),
+                  __uint_as_float(__float_as_uint(y.y) + (((uint32_t)b1 << 17) & 0xff800000u)));
+  // rounding test (the one-sided form of CRlibm, de Dinechin, Lauter and
+  // Muller): y = RN(y + er), and the exact value is within 2^-42 y of
+  // y + er; if y + er (1 + 2^-16) still rounds to y, so does every value
+  // within 2^-42 y of y + er (2^-42 y (1 + 2^16) stays below the distance
+  // from y to the nearest midpoint for y in [0.99, 2.02])
+  const float kE = __int_as_float(0x3f800080);  // 1 + 2^-16
+  const float2 chk = fma2_rn(er, make_float2(kE, kE), y);
+  const bool ok0 = in0 && chk.x == y.x;
+  const bool ok1 = in1 && chk.y == y.y;
   if (ok0 && ok1) return res;
   return make_float2(ok0 ? res.x : exp_cr_slow(x.x), ok1 ? res.y : exp_cr_slow(x.y));
 }
