@@ -25,7 +25,7 @@
 //   * y + er = T (1 + (e^r - 1)) with error below 2^-46 relative; y is the
 //     correctly rounded result when y + er (1 + 2^-16) rounds to y (a
 //     rounding test with a 16-fold margin on that bound), which fails for
-//     about one argument in 2^16; those arguments go to fp64 exp rounded
+//     about one argument in 2^17; those arguments go to fp64 exp rounded
 //     once, as do NaN and |x| > 86. Arguments <= -104 (e^x < 2^-150, half
 //     the smallest subnormal) give +0.
 //   * The result is y 2^k (exact: y 2^k is normal for k >= -125).
