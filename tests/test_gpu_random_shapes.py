@@ -47,3 +47,24 @@ def test_random_shape(seed):
     print(seed, (case.ratio, case.coff, case.head_dim, len(case.seqlens), case.total_tokens,
                  case.capacity), {k: (v if not isinstance(v, dict) else (v["differing"], v["max_abs"]))
                                   for k, v in res.items()})
+
+
+EXACT_SHAPES = ((2, 1), (4, 1), (8, 1), (2, 2), (4, 2))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shape_exact(seed):
+    """The exact mode on seeded random shapes of its envelope (windows of at
+    most 8 slots): out, dkv and dscore carry the oracle's bits."""
+    from test_gpu_exact import check_exact
+    rng = np.random.default_rng(5000 + seed)
+    ratio, coff = EXACT_SHAPES[int(rng.integers(0, len(EXACT_SHAPES)))]
+    d = int(rng.choice(HEAD_DIMS))
+    nseg = int(rng.integers(1, 12))
+    hi = max(2, min(3_000_000 // (coff * ratio * d) * ratio // nseg, 400 * ratio))
+    lens = rng.integers(0, hi, nseg)
+    lens[rng.integers(0, nseg)] = max(int(lens.max()), ratio)
+    case = workloads.make_case(f"xrand{seed}", lens.tolist(), ratio, coff, d,
+                               pad_rows=int(rng.integers(0, 6)),
+                               extra_tokens=int(rng.integers(0, 2 * ratio)), seed=100 + seed)
+    print(seed, (ratio, coff, d, len(lens), case.total_tokens), check_exact(case))
