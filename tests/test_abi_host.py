@@ -136,3 +136,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         binding.load()
+
+
+def test_plain_c_client(lib, tmp_path):
+    """include/csa_compress.h compiles as C99 and a C program linked against
+    libcsa_compress.so gets the documented status codes (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from gated_softmax_kv_gb300 import nvbuild
+    build_dir = os.path.dirname(nvbuild.LIB)
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(nvbuild.nvcc())), "include")
+    exe = str(tmp_path / "abi_client")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, os.path.join(ROOT, "tests", "abi_client.c"), "-L", build_dir,
+                    "-lcsa_compress", "-Wl,-rpath," + build_dir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("ok")
