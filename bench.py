@@ -236,10 +236,17 @@ def oracle_rate(case, budget_s: float = 12.0, min_tokens: int = 16384):
     per_token = t_cal / cal.total_tokens
     tokens = int(min(case.total_tokens, max(min_tokens, budget_s / per_token)))
     sample = sub_case(tokens)
+    # when the whole workload takes less than the budget, repeat it until
+    # about that much CPU time has been measured
     t = run(sample)
-    return sample.total_tokens / t, cores, (
+    passes = 1
+    while t < 0.8 * budget_s and passes < 64:
+        t += run(sample)
+        passes += 1
+    return passes * sample.total_tokens / t, cores, (
         f"first {len(sample.seqlens)} segments of the workload ({sample.total_tokens} tokens, "
-        f"{sample.capacity} rows incl. proportional padding), O32 fwd + bwd once, {t:.1f} s"), sample
+        f"{sample.capacity} rows incl. proportional padding), O32 fwd + bwd, "
+        f"{passes} pass{'es' if passes > 1 else ''}, {t:.1f} s"), sample
 
 
 # ------------------------------------------------------------------ arms
