@@ -92,42 +92,73 @@ def csa_compress_bwd_ptr(kv: int, score: int, ape: int, cu_seqlens: int, cu_seql
 # ------------------------------------------------------------- torch tensors
 
 
-def _check(t, name, dtype, device, ndim=None):
+def _check_detail(t, name, dtype, dev, ndim):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+    if t.get_device() != dev:
+        raise ValueError(f"{name} is on {t.device}, expected cuda:{dev}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims")
+    raise ValueError(f"{name} is not a valid argument")
 
 
-def _stream_handle(stream, device) -> int:
+def _check(t, name, dtype, dev: int, ndim=None):
+    """dtype, CUDA device index, contiguity and rank in one test (tensor
+    attribute reads dominate the host cost of a call); the specific error is
+    worked out only when the test fails."""
+    try:
+        ok = (t.dtype is dtype and t.get_device() == dev and t.is_contiguous()
+              and (ndim is None or t.dim() == ndim))
+    except AttributeError:
+        ok = False
+    if not ok:
+        _check_detail(t, name, dtype, dev, ndim)
+
+
+_raw_stream = None
+
+
+def _stream_handle(stream, dev: int) -> int:
+    """The CUDA stream to launch on: `stream`, else the current stream of the
+    device (read as a raw handle where torch offers that, which avoids
+    building a Stream object per call)."""
+    global _raw_stream
+    if stream is not None:
+        return int(stream.cuda_stream)
     import torch
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return int(stream.cuda_stream)
+    if _raw_stream is None:
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _raw_stream:
+        return int(_raw_stream(dev))
+    return int(torch.cuda.current_stream(dev).cuda_stream)
 
 
 def _shapes(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim):
     import torch
-    dev = kv.device
+    dev = kv.get_device() if isinstance(kv, torch.Tensor) else -1
+    if dev < 0:  # also rejects CPU tensors: the kernels take device pointers
+        _check_detail(kv, "kv", torch.bfloat16, 0, 2)
     _check(kv, "kv", torch.bfloat16, dev, 2)
     _check(score, "score", torch.bfloat16, dev, 2)
     _check(ape, "ape", torch.float32, dev, 2)
     _check(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
     _check(cu_seqlens_comp, "cu_seqlens_comp", torch.int32, dev, 1)
-    if kv.shape != score.shape or kv.shape[1] != coff * head_dim:
+    ks = kv.shape
+    if ks != score.shape or ks[1] != coff * head_dim:
         raise ValueError("kv and score must both be [total_tokens, coff*head_dim]")
-    if tuple(ape.shape) != (ratio, coff * head_dim):
+    if ape.shape != (ratio, coff * head_dim):
         raise ValueError("ape must be [ratio, coff*head_dim]")
-    if cu_seqlens.shape != cu_seqlens_comp.shape or cu_seqlens.numel() < 2:
+    n = cu_seqlens.shape[0]
+    if cu_seqlens_comp.shape[0] != n or n < 2:
         raise ValueError("cu_seqlens and cu_seqlens_comp must both be [num_seqs + 1]")
-    return dev, int(cu_seqlens.numel() - 1), int(kv.shape[0])
+    return dev, n - 1, ks[0]
 
 
 def csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, capacity: int, ratio: int,

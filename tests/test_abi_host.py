@@ -156,3 +156,19 @@ def test_plain_c_client(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok")
+
+
+def test_binding_rejects_host_tensors():
+    """The kernels take device pointers: the binding refuses CPU tensors before
+    anything reaches the library."""
+    torch = pytest.importorskip("torch")
+    kv = torch.zeros(8, 128, dtype=torch.bfloat16)
+    ape = torch.zeros(4, 128, dtype=torch.float32)
+    cu = torch.tensor([0, 8], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gsk.csa_compress_fwd(kv, kv, ape, cu, torch.tensor([0, 2], dtype=torch.int32), 2, 4, 2, 64)
+    with pytest.raises(TypeError):
+        gsk.csa_compress_fwd(kv.float(), kv, ape, cu, cu, 2, 4, 2, 64)
+    go = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gsk.csa_compress_bwd(kv, kv, ape, cu, cu, 2, 4, 2, 64, go)
