@@ -241,13 +241,13 @@ def main(argv=None) -> int:
     ap = argparse.ArgumentParser(prog="python -m gated_softmax_kv_gb300.ncu_harness")
     sub = ap.add_subparsers(dest="cmd", required=True)
     a = sub.add_parser("launches")
-    a.add_argument("--out", default="gpurun_out/launches.csv")
+    a.add_argument("--out", default="ncu_out/launches.csv")
     a.add_argument("--count", type=int, default=60)
     c = sub.add_parser("capture")
     c.add_argument("--kernels", default=r"(fwd|bwd)_small|dape_reduce")
     c.add_argument("--skip", type=int, default=3)
     c.add_argument("--count", type=int, default=3)
-    c.add_argument("--out", default="gpurun_out/prof_small")
+    c.add_argument("--out", default="ncu_out/prof_small")
     t = sub.add_parser("traffic")
     t.add_argument("report")
     t.add_argument("--tokens", type=int, required=True)
