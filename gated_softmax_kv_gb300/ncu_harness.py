@@ -31,7 +31,6 @@ from __future__ import annotations
 import argparse
 import collections
 import csv
-import io
 import json
 import os
 import re
