@@ -114,3 +114,46 @@ def test_two_host_threads_on_two_streams(gsk):
         for rep in results[i]:
             for a, b in zip(alone[i], rep):
                 assert np.array_equal(a, b)
+
+
+def test_two_host_threads_on_two_streams_exact_mode(gsk):
+    """The same for the exact mode's kernels (its own launch shapes and
+    workspace sizes): concurrent calls on two streams give the bits of the
+    same calls made alone."""
+    import threading
+    cases = [workloads.config("r4d512"), workloads.config("r2d128rag")]
+    dev = []
+    for case in cases:
+        dev.append(dict(kv=_bf16(case.kv), score=_bf16(case.score), go=_bf16(case.grad_out),
+                        ape=torch.from_numpy(case.ape).cuda(),
+                        cu=torch.from_numpy(case.cu_seqlens).cuda(),
+                        cuc=torch.from_numpy(case.cu_seqlens_comp).cuda()))
+    torch.cuda.synchronize()
+
+    def run(i, stream):
+        c, t = cases[i], dev[i]
+        meta = (c.capacity, c.ratio, c.coff, c.head_dim)
+        with torch.cuda.stream(stream):
+            out = gsk.csa_compress_fwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"], *meta,
+                                       stream=stream, exact=True)
+            dkv, ds, dape = gsk.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
+                                                 *meta, t["go"], stream=stream, exact=True)
+        stream.synchronize()
+        return [_bits(x) for x in (out, dkv, ds, dape)]
+
+    alone = [run(i, torch.cuda.Stream()) for i in range(2)]
+    results = {}
+
+    def worker(i):
+        s = torch.cuda.Stream()
+        results[i] = [run(i, s) for _ in range(3)]
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    for i in range(2):
+        for rep in results[i]:
+            for a, b in zip(alone[i], rep):
+                assert np.array_equal(a, b)
