@@ -47,6 +47,8 @@ def load() -> ctypes.CDLL:
     lib.csa_compress_fwd_exact.restype = ctypes.c_int
     lib.csa_compress_bwd_exact.argtypes = common + [vp, vp, vp, vp, vp]
     lib.csa_compress_bwd_exact.restype = ctypes.c_int
+    lib.csa_check_segments.argtypes = [vp, vp, i32, i64, i64, i32, vp, vp]
+    lib.csa_check_segments.restype = ctypes.c_int
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_cuda_error.argtypes = []
@@ -232,3 +234,39 @@ def csa_compress_bwd_noalloc_ptr(kv: int, score: int, ape: int, cu_seqlens: int,
             coff, head_dim, grad_out, dkv, dscore, dape, stream)
     if st != 0:
         _raise(st)
+
+
+# ------------------------------------------------------------- segment check
+
+SEG_VIOLATIONS = {1: "cu_seqlens[0] or cu_seqlens_comp[0] is not 0",
+                  2: "cu_seqlens decreases",
+                  4: "cu_seqlens_comp does not step by floor(seqlen / ratio)",
+                  8: "cu_seqlens[-1] > total_tokens",
+                  16: "cu_seqlens_comp[-1] > capacity (rows past capacity get no output slot)"}
+
+
+def csa_check_segments(cu_seqlens, cu_seqlens_comp, total_tokens: int, capacity: int, ratio: int,
+                       stream=None) -> int:
+    """The device-side preconditions of the segment arrays (csa_check_segments):
+    returns the bitmask of violations, 0 when they all hold. Reads the result
+    back, so it synchronises the stream: a debugging aid, not for the hot loop."""
+    import torch
+    dev = cu_seqlens.get_device() if isinstance(cu_seqlens, torch.Tensor) else -1
+    if dev < 0:
+        _check_detail(cu_seqlens, "cu_seqlens", torch.int32, 0, 1)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    _check(cu_seqlens_comp, "cu_seqlens_comp", torch.int32, dev, 1)
+    n = cu_seqlens.shape[0]
+    if cu_seqlens_comp.shape[0] != n or n < 2:
+        raise ValueError("cu_seqlens and cu_seqlens_comp must both be [num_seqs + 1]")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.stream(stream):
+        word = torch.zeros(1, dtype=torch.int32, device=dev)  # zeroed in stream order
+    st = load().csa_check_segments(cu_seqlens.data_ptr(), cu_seqlens_comp.data_ptr(), n - 1,
+                                   total_tokens, capacity, ratio, word.data_ptr(),
+                                   int(stream.cuda_stream))
+    if st != 0:
+        _raise(st)
+    stream.synchronize()
+    return int(word.cpu()[0])

@@ -42,8 +42,9 @@
  *   total_tokens >= ratio, 16-byte aligned kv/score/ape/out/grad_out/dkv/
  *   dscore/dape and 4-byte aligned segment arrays, no null pointer.
  *
- * Device-side preconditions (not checked: checking them would need a host
- * synchronisation): cu_seqlens and cu_seqlens_comp start at 0 and do not
+ * Device-side preconditions (not checked by the compute calls: checking them
+ * would need a host synchronisation; csa_check_segments below checks them on
+ * request): cu_seqlens and cu_seqlens_comp start at 0 and do not
  * decrease, cu_seqlens[num_seqs] <= total_tokens,
  * cu_seqlens_comp[s+1] - cu_seqlens_comp[s] == floor(seqlen_s / ratio).
  * When they do not hold the kernels still stay inside the buffers described
@@ -169,6 +170,33 @@ csa_status_t csa_compress_bwd_exact(const void* kv, const void* score, const flo
                                     int32_t ratio, int32_t coff, int32_t head_dim,
                                     const void* grad_out, void* dkv, void* dscore, float* dape,
                                     cudaStream_t stream);
+
+/*
+ * Checks the device-side preconditions on the segment arrays (the ones the
+ * compute calls trust) and ORs a bit per kind of violation into *violations,
+ * a caller-owned int32 in device memory that the caller zeroes first and
+ * reads after synchronising the stream:
+ *   CSA_SEG_BAD_START    cu_seqlens[0] != 0 or cu_seqlens_comp[0] != 0
+ *   CSA_SEG_DECREASING   cu_seqlens decreases somewhere
+ *   CSA_SEG_BAD_COMP     cu_seqlens_comp[s+1] - cu_seqlens_comp[s] !=
+ *                        floor(seqlen_s / ratio) for some segment s
+ *   CSA_SEG_PAST_END     cu_seqlens[num_seqs] > total_tokens
+ *   CSA_SEG_OVER_CAPACITY cu_seqlens_comp[num_seqs] > capacity (allowed: rows
+ *                        past capacity get no output slot; reported for
+ *                        callers that want to know)
+ * One kernel launch, asynchronous on `stream`, no host synchronisation; the
+ * result is the same whatever the order the threads run in. Arguments are
+ * validated as in the compute calls (num_seqs >= 1, ratio in the envelope,
+ * sizes non-negative, 4-byte aligned non-null pointers).
+ */
+#define CSA_SEG_BAD_START 1
+#define CSA_SEG_DECREASING 2
+#define CSA_SEG_BAD_COMP 4
+#define CSA_SEG_PAST_END 8
+#define CSA_SEG_OVER_CAPACITY 16
+csa_status_t csa_check_segments(const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
+                                int32_t num_seqs, int64_t total_tokens, int64_t capacity,
+                                int32_t ratio, int32_t* violations, cudaStream_t stream);
 
 /* Static description of a status code (never null). */
 const char* csa_status_string(csa_status_t status);

@@ -53,6 +53,8 @@ int main(void) {
   expect("bwd_exact: ratio 8, coff 2",
          csa_compress_bwd_exact(a, a, ape, seg, seg, 1, 256, 8, 8, 2, 64, a, a, a, (float*)a, 0),
          CSA_ERR_UNSUPPORTED);
+  expect("check_segments: null violations word",
+         csa_check_segments(seg, seg, 1, 64, 8, 4, NULL, 0), CSA_ERR_NULL);
   if (strcmp(csa_status_string((csa_status_t)99), "unknown status") != 0) ++failures;
   if (csa_last_cuda_error() != 0) ++failures;
   printf("%s\n", failures ? "FAILED" : "ok");

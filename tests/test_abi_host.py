@@ -172,3 +172,15 @@ def test_binding_rejects_host_tensors():
     go = torch.zeros(2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         gsk.csa_compress_bwd(kv, kv, ape, cu, cu, 2, 4, 2, 64, go)
+
+
+def test_segment_check_validation(lib):
+    # rejected before any CUDA call
+    seg = ctypes.c_void_p(A)
+    f = lib.csa_check_segments
+    assert f(seg, seg, 1, 64, 8, 3, seg, None) == 3          # ratio 3
+    assert f(seg, seg, 0, 64, 8, 4, seg, None) == 4          # num_seqs 0
+    assert f(seg, seg, 1, -1, 8, 4, seg, None) == 4
+    assert f(None, seg, 1, 64, 8, 4, seg, None) == 1
+    assert f(seg, seg, 1, 64, 8, 4, None, None) == 1
+    assert f(seg, ctypes.c_void_p(A + 2), 1, 64, 8, 4, seg, None) == 2
