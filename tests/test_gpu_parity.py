@@ -192,3 +192,34 @@ def test_parity_page_packs(name):
     res = check_case(workloads.config(name))
     print(name, {k: (v if not isinstance(v, dict) else (v["differing"], v["max_abs"]))
                  for k, v in res.items()})
+
+
+@pytest.mark.parametrize("ratio,coff", [(4, 2), (128, 1)])
+def test_rows_past_capacity(ratio, coff):
+    """cu_seqlens_comp[-1] > capacity: the forward writes the capacity rows,
+    which equal the oracle's first rows; in the backward the rows without an
+    output slot count as rows with zero gradient (the oracle's result with
+    their grad_out zeroed), and every position is still written."""
+    case = workloads.make_case("over", [8 * ratio + 1, 5 * ratio, 3 * ratio + 2], ratio, coff, 64,
+                               extra_tokens=3, seed=13)
+    R = case.true_rows
+    C = R - 5
+    full = problem(case)
+    o_out = oracle.fwd32(full, case.kv, case.score, case.ape)
+    go = case.grad_out.copy()
+    go[C:] = 0
+    o_dkv, o_ds, o_dape = oracle.bwd32(full, case.kv, case.score, case.ape, go)
+
+    cut = workloads.make_case("over", list(case.seqlens), ratio, coff, 64, extra_tokens=3, seed=13,
+                              fill=False)
+    cut.kv, cut.score, cut.ape = case.kv, case.score, case.ape
+    cut.capacity = C
+    cut.grad_out = case.grad_out[:C].copy()
+    dc = _dev(cut)
+    out = dc.fwd(prefill=0x7FC0)
+    dkv, ds, dape = dc.bwd(prefill=0x7FC0)
+    gate_bf16(out, o_out[:C], "out")
+    gate_bf16(dkv, o_dkv, "dkv")
+    gate_bf16(ds, o_ds, "dscore")
+    scale = max(float(np.max(np.abs(o_dape))), 1e-30)
+    assert float(np.max(np.abs(dape.astype(np.float64) - o_dape))) / scale <= 1e-5
