@@ -184,3 +184,39 @@ def test_segment_check_validation(lib):
     assert f(None, seg, 1, 64, 8, 4, seg, None) == 1
     assert f(seg, seg, 1, 64, 8, 4, None, None) == 1
     assert f(seg, ctypes.c_void_p(A + 2), 1, 64, 8, 4, seg, None) == 2
+
+
+def _expected_status(nseq, T, C, r, coff, d, ptrs_ok=True):
+    """The envelope of include/csa_compress.h, written out from its comment."""
+    if r not in (2, 4, 8, 16, 32, 64, 128) or coff not in (1, 2):
+        return 3
+    if d < 8 or d % 8 != 0:
+        return 3
+    if nseq < 1 or T < 0 or C < 0:
+        return 4
+    if T * coff * d >= (1 << 31) or C * d >= (1 << 31):
+        return 4
+    if C > 0 and T < r:
+        return 4
+    return 0
+
+
+def test_forward_validation_matches_the_documented_envelope(lib):
+    """Seeded random argument tuples, valid and invalid: the forward's status
+    is the one the header's envelope gives (no call launches anything: valid
+    tuples use capacity 0)."""
+    import numpy as np
+    rng = np.random.default_rng(17)
+    for _ in range(3000):
+        r = int(rng.choice([0, 1, 2, 3, 4, 8, 16, 32, 64, 128, 256]))
+        coff = int(rng.integers(0, 4))
+        d = int(rng.choice([0, 4, 8, 12, 64, 512, 1024, 4096, 1 << 20]))
+        nseq = int(rng.integers(-1, 4))
+        T = int(rng.choice([-1, 0, 1, 3, 64, 1 << 20, 1 << 30]))
+        C = int(rng.choice([-1, 0, 1, 8, 1 << 22]))
+        want = _expected_status(nseq, T, C, r, coff, d)
+        if want == 0:
+            C = 0  # keep the call launch-free
+            want = _expected_status(nseq, T, C, r, coff, d)
+        got = fwd(lib, nseq=nseq, T=T, C=C, r=r, coff=coff, d=d, out=0 if C == 0 else A)
+        assert got == want, (nseq, T, C, r, coff, d, got, want)
