@@ -23,6 +23,12 @@ namespace {
 #endif
 // Long-window backward: windows of at least this many slots give each warp 16
 // slots x 2 columns (8-warp CTAs, two per SM) instead of 8 slots x 4 columns.
+// 1: kv / score / grad_out loads skip L1 allocation, so the L1 keeps the APE
+// tile the threads re-read every row (ratio 128: 1.3% faster at 131072 tokens,
+// coff 1, head_dim 512; 0: streaming loads)
+#ifndef CSA_BWD_LONG_NOALLOC
+#define CSA_BWD_LONG_NOALLOC 1
+#endif
 #ifndef CSA_BWD_LONG_KPT16_FROM
 #define CSA_BWD_LONG_KPT16_FROM 128
 #endif
@@ -62,7 +68,15 @@ struct ColVec;
 template <>
 struct ColVec<2> {
   using T = uint32_t;
+#if CSA_BWD_LONG_NOALLOC
+  static __device__ __forceinline__ T load(const uint16_t* p) {
+    uint32_t v;
+    asm("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+  }
+#else
   static __device__ __forceinline__ T load(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint32_t*>(p)); }
+#endif
   static __device__ __forceinline__ void store(uint16_t* p, T v) { __stcs(reinterpret_cast<uint32_t*>(p), v); }
   static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(v, c); }
   static __device__ __forceinline__ T zero() { return 0u; }
@@ -87,7 +101,15 @@ struct ColVec<2> {
 template <>
 struct ColVec<4> {
   using T = uint2;
+#if CSA_BWD_LONG_NOALLOC
+  static __device__ __forceinline__ T load(const uint16_t* p) {
+    uint2 v;
+    asm("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+  }
+#else
   static __device__ __forceinline__ T load(const uint16_t* p) { return ld_stream8(p); }
+#endif
   static __device__ __forceinline__ void store(uint16_t* p, T v) { st_stream8(p, v); }
   static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(c < 2 ? v.x : v.y, c & 1); }
   static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
