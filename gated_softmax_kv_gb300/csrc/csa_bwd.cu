@@ -307,7 +307,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   auto kern = bwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
-  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  int64_t gy = (int64_t)kGroupingSms * occ / tiles;
   const int64_t row_blocks = (p.C + ty - 1) / ty;
   if (gy > row_blocks) gy = row_blocks;
   if (gy < 1) gy = 1;

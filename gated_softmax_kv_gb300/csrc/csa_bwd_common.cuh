@@ -10,6 +10,12 @@
 
 namespace csa {
 
+// The backward kernels' row-group count (the number of dAPE partials) is
+// sized for this many SMs, not for the device's own count, so the grouping
+// and with it dape's bits depend on the problem alone on every sm_103a part
+// (152 is GB300's count; on a part with fewer SMs the few extra CTAs queue).
+constexpr int kGroupingSms = 152;
+
 // Zeros for the positions no row reads that belong to nobody's window:
 // segments shorter than the ratio and tokens >= cu_seqlens[num_seqs].
 // Spread over every CTA of the launch.

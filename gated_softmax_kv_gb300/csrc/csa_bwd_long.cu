@@ -420,7 +420,7 @@ cudaError_t plan_long_d(const Problem& p, BwdShape* s) {
   constexpr size_t smem = sizeof(float) * W * 32 * LongShape<W>::kVc;  // dape sums of the tile
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), NT, smem);
-  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  int64_t gy = (int64_t)kGroupingSms * occ / tiles;
   if (gy > p.C) gy = p.C;
   if (gy < 1) gy = 1;
   // even out the rows per CTA

@@ -283,7 +283,7 @@ ExactShape exact_shape(int d) {
 // one per TY rows.
 int64_t exact_rows_grid(const void* kern, const ExactShape& s, size_t smem, int64_t rows) {
   const int occ = occupancy(kern, s.tx * s.ty, smem);
-  int64_t gy = (int64_t)sm_count() * occ / s.tiles;
+  int64_t gy = (int64_t)kGroupingSms * occ / s.tiles;
   const int64_t row_blocks = (rows + s.ty - 1) / s.ty;
   if (gy > row_blocks) gy = row_blocks;
   if (gy < 1) gy = 1;

@@ -95,10 +95,10 @@ csa_status_t csa_compress_fwd(const void* kv, const void* score, const float* ap
  *   dape        -- OVERWRITTEN (not accumulated) with the sum over non-padding
  *                  rows of every window slot's fp32 logit gradient, reduced in
  *                  a fixed order (per-block fp32 partials, then an ordered
- *                  final sum): bitwise run-to-run deterministic, no atomics
- *                  (the row grouping follows the grid, which is sized from
- *                  the SM count: GPUs with another SM count may differ in the
- *                  last bits; out, dkv and dscore depend on the problem only).
+ *                  final sum): bitwise run-to-run deterministic, no atomics;
+ *                  the row grouping, like every other choice that orders
+ *                  the arithmetic, depends on the problem only, never on the
+ *                  device's SM count.
  * grad_out rows >= cu_seqlens_comp[num_seqs] are never read.
  * Two kernel launches. The dape partials live in a stream-ordered workspace
  * taken from a library-owned CUDA memory pool on `stream` (released on the
