@@ -29,6 +29,12 @@ namespace {
 #ifndef CSA_BWD_LONG_NOALLOC
 #define CSA_BWD_LONG_NOALLOC 1
 #endif
+// 1: dkv / dscore stores skip L1 allocation too and keep the normal L2 policy
+// (ratio 128: 2.3% faster backward at 131072 tokens, coff 1, head_dim 512;
+// 0: evict-first stores)
+#ifndef CSA_BWD_LONG_NOALLOC_ST
+#define CSA_BWD_LONG_NOALLOC_ST 1
+#endif
 #ifndef CSA_BWD_LONG_KPT16_FROM
 #define CSA_BWD_LONG_KPT16_FROM 128
 #endif
@@ -77,7 +83,13 @@ struct ColVec<2> {
 #else
   static __device__ __forceinline__ T load(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint32_t*>(p)); }
 #endif
+#if CSA_BWD_LONG_NOALLOC_ST
+  static __device__ __forceinline__ void store(uint16_t* p, T v) {
+    asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+  }
+#else
   static __device__ __forceinline__ void store(uint16_t* p, T v) { __stcs(reinterpret_cast<uint32_t*>(p), v); }
+#endif
   static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(v, c); }
   static __device__ __forceinline__ T zero() { return 0u; }
   static __device__ __forceinline__ T ninf() { return kNegInfBf16x2; }

@@ -163,8 +163,12 @@ __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
+// Streaming stores of out / dkv / dscore: no L1 line and the normal L2 policy
+// (measured 1.0% faster backward at the headline than the evict-first .cs
+// form, which the plain form was not).
 __device__ __forceinline__ void st_stream(uint16_t* p, uint4 v) {
-  __stcs(reinterpret_cast<uint4*>(p), v);
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 __device__ __forceinline__ uint2 ld_stream8(const uint16_t* p) {
   uint2 v;
@@ -172,7 +176,8 @@ __device__ __forceinline__ uint2 ld_stream8(const uint16_t* p) {
   return v;
 }
 __device__ __forceinline__ void st_stream8(uint16_t* p, uint2 v) {
-  __stcs(reinterpret_cast<uint2*>(p), v);
+  asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y)
+               : "memory");
 }
 __device__ __forceinline__ float4 ld_f4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
