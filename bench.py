@@ -203,7 +203,8 @@ class ClockSampler:
 
 def oracle_rate(case, budget_s: float = 12.0, min_tokens: int = 16384):
     """Tokens/s of the CPU oracle (fp32 fwd + bwd, all host cores) on a prefix
-    of the workload's segments sized from a short calibration run."""
+    of the workload's segments sized from a short calibration run, and the
+    single-thread rate on the calibration prefix."""
     import numpy as np
     import oracle
     import workloads
@@ -223,12 +224,12 @@ def oracle_rate(case, budget_s: float = 12.0, min_tokens: int = 16384):
         return workloads.make_case("sample", lens, case.ratio, case.coff, case.head_dim,
                                    pad_rows=pad, seed=1)
 
-    def run(c):
+    def run(c, nthreads=cores):
         p = oracle.Problem(c.cu_seqlens, c.cu_seqlens_comp, c.total_tokens, c.capacity,
                            c.ratio, c.coff, c.head_dim)
         t0 = time.perf_counter()
-        oracle.fwd32(p, c.kv, c.score, c.ape, nthreads=cores)
-        oracle.bwd32(p, c.kv, c.score, c.ape, c.grad_out, nthreads=cores)
+        oracle.fwd32(p, c.kv, c.score, c.ape, nthreads=nthreads)
+        oracle.bwd32(p, c.kv, c.score, c.ape, c.grad_out, nthreads=nthreads)
         return time.perf_counter() - t0
 
     cal = sub_case(min_tokens)
@@ -243,10 +244,15 @@ def oracle_rate(case, budget_s: float = 12.0, min_tokens: int = 16384):
     while t < 0.8 * budget_s and passes < 64:
         t += run(sample)
         passes += 1
+    # the calibration prefix once more on a single thread, beside its all-cores time
+    t1 = run(cal, nthreads=1)
+    single = {"value_1thread": cal.total_tokens / t1,
+              "sample_1thread": f"first {len(cal.seqlens)} segments ({cal.total_tokens} tokens), "
+                                f"O32 fwd + bwd: one thread {t1:.2f} s, all {cores} cores {t_cal:.2f} s"}
     return passes * sample.total_tokens / t, cores, (
         f"first {len(sample.seqlens)} segments of the workload ({sample.total_tokens} tokens, "
         f"{sample.capacity} rows incl. proportional padding), O32 fwd + bwd, "
-        f"{passes} pass{'es' if passes > 1 else ''}, {t:.1f} s"), sample
+        f"{passes} pass{'es' if passes > 1 else ''}, {t:.1f} s"), single
 
 
 # ------------------------------------------------------------------ arms
@@ -571,8 +577,9 @@ def run_gpu(args, rank, world, local):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, cores, desc, _ = oracle_rate(case)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        rate, cores, desc, single = oracle_rate(case)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               **single}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,

@@ -74,3 +74,14 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 
     assert bench.run_reference(A(), rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    case = workloads.make_case("tiny", [37, 64, 19, 200], 4, 2, 64, pad_rows=4, seed=0)
+    rate, cores, desc, single = bench.oracle_rate(case, budget_s=0.05, min_tokens=64)
+    assert rate > 0 and cores >= 1 and "O32 fwd + bwd" in desc
+    assert single["value_1thread"] > 0
+    assert "one thread" in single["sample_1thread"]
