@@ -85,3 +85,23 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert rate > 0 and cores >= 1 and "O32 fwd + bwd" in desc
     assert single["value_1thread"] > 0
     assert "one thread" in single["sample_1thread"]
+
+
+def test_reference_arm_line_carries_the_contract_keys(capsys):
+    import json
+    import bench
+
+    class A:
+        steps, warmup, tokens, workload = 1, 1, 4096, "headline"
+
+    assert bench.run_reference(A(), rank=0, world=1) in (0, None)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
