@@ -47,6 +47,8 @@ def load() -> ctypes.CDLL:
     lib.csa_compress_fwd_exact.restype = ctypes.c_int
     lib.csa_compress_bwd_exact.argtypes = common + [vp, vp, vp, vp, vp]
     lib.csa_compress_bwd_exact.restype = ctypes.c_int
+    lib.csa_compress_bwd_noalloc.argtypes = common + [vp, vp, vp, vp, vp]
+    lib.csa_compress_bwd_noalloc.restype = ctypes.c_int
     lib.csa_check_segments.argtypes = [vp, vp, i32, i64, i64, i32, vp, vp]
     lib.csa_check_segments.restype = ctypes.c_int
     lib.csa_status_string.argtypes = [ctypes.c_int]
@@ -226,10 +228,6 @@ def csa_compress_bwd_noalloc_ptr(kv: int, score: int, ape: int, cu_seqlens: int,
     problem needs more than that."""
     lib = load()
     fn = lib.csa_compress_bwd_noalloc
-    if fn.argtypes is None:
-        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-        fn.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp]
-        fn.restype = ctypes.c_int
     st = fn(kv, score, ape, cu_seqlens, cu_seqlens_comp, num_seqs, total_tokens, capacity, ratio,
             coff, head_dim, grad_out, dkv, dscore, dape, stream)
     if st != 0:

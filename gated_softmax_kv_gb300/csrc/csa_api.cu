@@ -61,17 +61,26 @@ csa::Problem make_problem(const void* kv, const void* score, const float* ape, c
   return p;
 }
 
-// One pool per device for the dape partials. The release threshold keeps the
-// memory cached between calls, so steady-state calls do not map new memory.
+// One pool per CUDA context for the dape partials. The release threshold
+// keeps the memory cached between calls, so steady-state calls do not map
+// new memory. The cache is keyed by the context id: after a device reset the
+// next call creates a pool in the new context instead of using the old one.
 cudaError_t workspace_pool(cudaMemPool_t* out) {
   static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
+  struct Entry {
+    unsigned long long ctx;
+    cudaMemPool_t pool;
+  };
+  static Entry pools[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  e = csa::current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (!pools[dev]) {
+  if (!pools[dev].pool || pools[dev].ctx != ctx) {
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
@@ -82,9 +91,10 @@ cudaError_t workspace_pool(cudaMemPool_t* out) {
     uint64_t keep = UINT64_MAX;
     e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
     if (e != cudaSuccess) return e;
-    pools[dev] = pool;
+    pools[dev].pool = pool;
+    pools[dev].ctx = ctx;
   }
-  *out = pools[dev];
+  *out = pools[dev].pool;
   return cudaSuccess;
 }
 
@@ -177,6 +187,56 @@ csa_status_t check_bwd_args(const void* kv, const void* score, const float* ape,
 }
 
 csa_status_t record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+namespace {
+
+// Driver entry points, looked up once through the runtime (no link against
+// libcuda): cuCtxGetCurrent and cuCtxGetId.
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+cudaError_t context_fns(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn s_cur = nullptr;
+  static CtxGetIdFn s_id = nullptr;
+  static cudaError_t s_err = cudaSuccess;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    s_err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q);
+    if (s_err == cudaSuccess && q != cudaDriverEntryPointSuccess) s_err = cudaErrorNotSupported;
+    if (s_err != cudaSuccess) return;
+    s_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+    s_err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q);
+    if (s_err == cudaSuccess && q != cudaDriverEntryPointSuccess) s_err = cudaErrorNotSupported;
+    if (s_err != cudaSuccess) return;
+    s_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  *cur = s_cur;
+  *id = s_id;
+  return s_err;
+}
+
+}  // namespace
+
+cudaError_t current_context_id(unsigned long long* out) {
+  CtxGetCurrentFn cur;
+  CtxGetIdFn getid;
+  cudaError_t e = context_fns(&cur, &getid);
+  if (e != cudaSuccess) return e;
+  void* ctx = nullptr;
+  if (cur(&ctx) != 0) return cudaErrorDeviceUninitialized;
+  if (!ctx) {
+    // no context current yet on this thread: let the runtime make the
+    // current device's primary context current (no memory is allocated)
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (cur(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+  }
+  return getid(ctx, out) == 0 ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
 
 }  // namespace csa
 

@@ -112,4 +112,12 @@ csa_status_t check_bwd_args(const void* kv, const void* score, const float* ape,
                             const float* dape);
 csa_status_t record_cuda_error(cudaError_t e);
 
+// The unique id of the CUDA context current on this thread (the driver's
+// context id, unique for the life of the process), creating the device's
+// primary context first if none is current. Host-side caches of per-context
+// objects (device symbol addresses, memory pools) are keyed by it, so that
+// a context destroyed and created again (cudaDeviceReset) is never served a
+// stale handle.
+cudaError_t current_context_id(unsigned long long* id);
+
 }  // namespace csa

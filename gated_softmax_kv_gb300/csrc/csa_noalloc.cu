@@ -10,9 +10,11 @@
 //
 // In host code `g_dape_scratch` names a host-side stand-in, not device
 // memory: the kernels get the device address that cudaGetSymbolAddress
-// returns, looked up once per device (with that device current) on the first
-// call there. Every call shares the array; calls whose kernels overlap on the
-// GPU race on it.
+// returns, looked up on the first call in each CUDA context of a device (with
+// that device current) and cached under the context's unique id, so that a
+// context destroyed and created again (cudaDeviceReset) makes the next call
+// look the address up again instead of launching with a stale one. Every
+// call shares the array; calls whose kernels overlap on the GPU race on it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,22 +30,31 @@ static_assert(kScratchFloats == 4 * 1024 * 1024, "scratch size is part of the do
 
 static __device__ __align__(256) float g_dape_scratch[kScratchFloats];
 
-// Device address of g_dape_scratch on the current device, looked up once per device.
+// Device address of g_dape_scratch in the current context, looked up once per
+// (device, context).
 cudaError_t scratch_address(float** out) {
   static std::mutex mu;
-  static float* addr[64] = {};
+  struct Entry {
+    unsigned long long ctx;
+    float* addr;
+  };
+  static Entry cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  e = csa::current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!cache[dev].addr || cache[dev].ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dape_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<float*>(p);
+    cache[dev].addr = static_cast<float*>(p);
+    cache[dev].ctx = ctx;
   }
-  *out = addr[dev];
+  *out = cache[dev].addr;
   return cudaSuccess;
 }
 

@@ -10,19 +10,25 @@ line without ncu and profiles only if that exits 0; ncu always gets
       time and share as a markdown table. Times under ncu are cold-cache and
       serialised: compare shares, not absolute times.
 
-  python -m gated_softmax_kv_gb300.ncu_harness capture --kernels REGEX [--skip N] [--count N]
+  python -m gated_softmax_kv_gb300.ncu_harness capture --kernel NAME [--skip N] [--count N]
           [--out NAME] [bench args...]
-      a --set full capture of a few launches of a small case (defaults: the
+      a --set full capture (plus the L2 read / write sector counts) of one to
+      three launches of ONE kernel (a plain function name such as
+      bwd_small_kernel, no alternation) on a small case (defaults: the
       headline recipe at 65536 tokens, above the L2 size but a few GB on the
-      device), then a table of the DRAM bytes, throughput, occupancy, issue
-      and pipe figures per captured kernel.
+      device), then a table of the DRAM bytes, stored bytes, throughput,
+      occupancy, issue and pipe figures per captured launch.
 
-  python -m gated_softmax_kv_gb300.ncu_harness traffic REPORT --tokens N
-      the per-token DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum)
-      of the forward and backward launches of a capture of the headline
-      recipe at N tokens, written to profiles/dram_traffic.json together with
-      a hash of the kernels' sources, which bench.py uses for
-      roofline.traffic while the sources are unchanged.
+  python -m gated_softmax_kv_gb300.ncu_harness traffic --fwd REPORT --bwd REPORT
+          --reduce REPORT --tokens N
+      the per-token bytes of the forward call (its kernel's capture) and of
+      the backward call (the backward kernel's capture plus the dape reduce's)
+      on the headline recipe at N tokens: DRAM reads, DRAM writes, and the
+      bytes stores wrote into L2 (lts__t_sectors_op_write.sum x 32, every one
+      of which is written back to DRAM, counted even when still dirty in L2
+      at the kernel's end), written to profiles/dram_traffic.json with a hash
+      of the kernels' sources, which bench.py uses for roofline.traffic while
+      the sources are unchanged.
 
 The parsing functions take ncu's CSV text and need no GPU.
 """
@@ -46,6 +52,8 @@ CAPTURE_METRICS = [
     ("gpu__time_duration.sum", "duration"),
     ("dram__bytes_read.sum", "DRAM read"),
     ("dram__bytes_write.sum", "DRAM write"),
+    ("lts__t_sectors_op_write.sum", "L2 write sectors (stores)"),
+    ("lts__t_sectors_op_read.sum", "L2 read sectors"),
     ("gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", "DRAM throughput (% of peak)"),
     ("launch__registers_per_thread", "registers / thread"),
     ("launch__occupancy_limit_registers", "blocks / SM (register limit)"),
@@ -60,15 +68,22 @@ CAPTURE_METRICS = [
     ("sm__inst_executed_pipe_xu.avg.pct_of_peak_sustained_active", "XU pipe (% of peak)"),
 ]
 
-# sources of the kernels whose traffic the record holds (csrc/ file names)
+# the L2 counters a capture adds to --set full (stores into L2, loads from L2)
+EXTRA_METRICS = "lts__t_sectors_op_write.sum,lts__t_sectors_op_read.sum"
+SECTOR_BYTES = 32
+
+# the calls whose traffic the record holds: the reports (one kernel each) that
+# make them up and the csrc/ sources of those kernels
 TRAFFIC_KERNELS = {
-    "csa_compress_fwd": dict(match=r"fwd_small_kernel", kernel="fwd_small_kernel<4,2,512>",
+    "csa_compress_fwd": dict(reports=["fwd"], kernel="fwd_small_kernel<4,2,512>",
                              sources=["csa_fwd.cu", "csa_device.cuh", "csa_internal.h"]),
-    "csa_compress_bwd": dict(match=r"bwd_small_kernel|dape_reduce_kernel",
+    "csa_compress_bwd": dict(reports=["bwd", "reduce"],
                              kernel="bwd_small_kernel<4,2,512> + dape_reduce_kernel",
                              sources=["csa_bwd.cu", "csa_bwd_common.cuh", "csa_device.cuh",
                                       "csa_internal.h"]),
 }
+
+_KERNEL_NAME = re.compile(r"[A-Za-z_][A-Za-z0-9_]*")
 
 _TIME_SCALE = {"nsecond": 1e-3, "ns": 1e-3, "usecond": 1.0, "us": 1.0, "msecond": 1e3, "ms": 1e3,
                "second": 1e6, "s": 1e6}
@@ -180,34 +195,56 @@ def capture_table(kernels) -> str:
     return "\n".join(out)
 
 
-def traffic_record(kernels, tokens: int, command: str) -> dict:
-    """Per-token DRAM bytes of the forward and backward launches of a capture
-    (the first launch of each kernel; the backward call is its kernel plus the
-    dAPE reduce)."""
-    first = collections.OrderedDict()
-    for k, vals in kernels:
-        first.setdefault(k, vals)
+def single_kernel_name(name: str) -> str:
+    """The --kernel argument of a capture: one plain function name (a full
+    capture of several kernels at once is not allowed)."""
+    if not _KERNEL_NAME.fullmatch(name or ""):
+        raise ValueError(f"--kernel takes one kernel's function name, not {name!r}")
+    return name
+
+
+def launch_bytes(vals) -> dict:
+    """DRAM reads, DRAM writes and bytes stored into L2 of one captured launch."""
+    rd = metric_value(vals, "dram__bytes_read.sum")
+    wr = metric_value(vals, "dram__bytes_write.sum")
+    st = metric_value(vals, "lts__t_sectors_op_write.sum")
+    if rd is None or wr is None or st is None:
+        raise ValueError("the capture lacks dram__bytes_read/write.sum or lts__t_sectors_op_write.sum")
+    return {"read": rd, "dram_write": wr, "l2_write": st * SECTOR_BYTES}
+
+
+def traffic_record(reports, tokens: int, command: str) -> dict:
+    """Per-token bytes of the forward and backward calls from single-kernel
+    captures: `reports` maps "fwd", "bwd" and "reduce" to parse_raw rows of
+    one kernel each (the first launch of each is used; the backward call is
+    its kernel plus the dape reduce). The traffic of a call is its DRAM reads
+    plus the bytes its stores wrote into L2 (all of which reach DRAM)."""
     import bench  # the source hash bench.py checks the record against
-    rec = {"note": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch from ncu --set full "
-                    "on the headline recipe scaled to %d tokens, divided by the tokens of that "
-                    "launch; bench.py scales it to the measured launch (traffic grows with the "
-                    "tokens: every token's kv and score are read once). Valid while the listed "
-                    "sources hash to source_hash. Bytes written that are still dirty in L2 when "
-                    "the kernel ends are not in the count. Command: %s" % (tokens, command))}
+    rec = {"note": ("per-token bytes of one launch per kernel from ncu --set full (plus "
+                    "lts__t_sectors_op_write.sum) on the headline recipe scaled to %d tokens, "
+                    "one capture per kernel; bench.py scales them to the measured launch (traffic "
+                    "grows with the tokens: every token's kv and score are read once). traffic = "
+                    "DRAM reads + bytes stored into L2 (every stored byte is written back; the DRAM "
+                    "write counter misses lines still dirty in L2 when the kernel ends). Valid while "
+                    "the listed sources hash to source_hash. Command: %s" % (tokens, command))}
     for key, spec in TRAFFIC_KERNELS.items():
-        total = 0.0
-        found = False
-        for k, vals in first.items():
-            if re.search(spec["match"], k):
-                rd = metric_value(vals, "dram__bytes_read.sum")
-                wr = metric_value(vals, "dram__bytes_write.sum")
-                if rd is None or wr is None:
-                    raise ValueError(f"{k}: the capture has no DRAM byte counters")
-                total += rd + wr
-                found = True
-        if not found:
-            raise ValueError(f"no launch of {spec['match']} in the capture")
-        rec[key] = dict(kernel=spec["kernel"], dram_bytes_per_unit=total / tokens, unit="token",
+        tot = {"read": 0.0, "dram_write": 0.0, "l2_write": 0.0}
+        names = []
+        for part in spec["reports"]:
+            rows = reports.get(part)
+            if not rows:
+                raise ValueError(f"no capture for the {part} kernel")
+            kernels = {k for k, _ in rows}
+            if len(kernels) != 1:
+                raise ValueError(f"the {part} capture holds {sorted(kernels)}: one kernel per capture")
+            names.append(rows[0][0])
+            for k, v in launch_bytes(rows[0][1]).items():
+                tot[k] += v
+        rec[key] = dict(kernel=" + ".join(names), unit="token",
+                        dram_read_bytes_per_unit=tot["read"] / tokens,
+                        dram_write_bytes_per_unit=tot["dram_write"] / tokens,
+                        l2_write_bytes_per_unit=tot["l2_write"] / tokens,
+                        dram_bytes_per_unit=(tot["read"] + tot["l2_write"]) / tokens,
                         sources=spec["sources"], source_hash=bench.source_hash(spec["sources"]))
     return rec
 
@@ -243,12 +280,15 @@ def main(argv=None) -> int:
     a.add_argument("--out", default="ncu_out/launches.csv")
     a.add_argument("--count", type=int, default=60)
     c = sub.add_parser("capture")
-    c.add_argument("--kernels", default=r"(fwd|bwd)_small|dape_reduce")
+    c.add_argument("--kernel", required=True,
+                   help="one kernel's function name, e.g. bwd_small_kernel")
     c.add_argument("--skip", type=int, default=3)
-    c.add_argument("--count", type=int, default=3)
-    c.add_argument("--out", default="ncu_out/prof_small")
+    c.add_argument("--count", type=int, default=1, choices=[1, 2, 3])
+    c.add_argument("--out", default="ncu_out/prof")
     t = sub.add_parser("traffic")
-    t.add_argument("report")
+    t.add_argument("--fwd", required=True)
+    t.add_argument("--bwd", required=True)
+    t.add_argument("--reduce", required=True)
     t.add_argument("--tokens", type=int, required=True)
     t.add_argument("--command", default="")
     args, rest = ap.parse_known_args(argv)
@@ -264,16 +304,21 @@ def main(argv=None) -> int:
         bench_args = rest or ["--tokens", "65536", "--steps", "2", "--warmup", "1", "--no-cpu-baseline",
                               "--e2e-steps", "1"]
         os.makedirs(os.path.dirname(os.path.join(ROOT, args.out)), exist_ok=True)
-        _plain_then(_bench(bench_args), ["--set", "full", "-k", "regex:" + args.kernels,
+        kernel = single_kernel_name(args.kernel)
+        _plain_then(_bench(bench_args), ["--set", "full", "--metrics", EXTRA_METRICS,
+                                         "-k", "regex:" + kernel,
                                          "-s", str(args.skip), "-c", str(args.count),
                                          "-o", os.path.join(ROOT, args.out)])
         raw = subprocess.run([_ncu(), "-i", os.path.join(ROOT, args.out) + ".ncu-rep", "--page", "raw",
                               "--csv"], capture_output=True, text=True, check=True).stdout
         print(capture_table(parse_raw(raw)))
     else:
-        raw = subprocess.run([_ncu(), "-i", args.report, "--page", "raw", "--csv"],
-                             capture_output=True, text=True, check=True).stdout
-        rec = traffic_record(parse_raw(raw), args.tokens, args.command)
+        reports = {}
+        for part in ("fwd", "bwd", "reduce"):
+            raw = subprocess.run([_ncu(), "-i", getattr(args, part), "--page", "raw", "--csv"],
+                                 capture_output=True, text=True, check=True).stdout
+            reports[part] = parse_raw(raw)
+        rec = traffic_record(reports, args.tokens, args.command)
         with open(TRAFFIC, "w") as f:
             json.dump(rec, f, indent=1)
             f.write("\n")

@@ -102,7 +102,9 @@ csa_status_t csa_compress_fwd(const void* kv, const void* score, const float* ap
  * grad_out rows >= cu_seqlens_comp[num_seqs] are never read.
  * Two kernel launches. The dape partials live in a stream-ordered workspace
  * taken from a library-owned CUDA memory pool on `stream` (released on the
- * stream after use, kept cached by the pool).
+ * stream after use, kept cached by the pool). The pool belongs to the CUDA
+ * context current at the call; after a device reset the next call makes a new
+ * one.
  */
 csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ape,
                               const int32_t* cu_seqlens, const int32_t* cu_seqlens_comp,
@@ -124,16 +126,21 @@ csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ap
  * live in one fixed array of CSA_NOALLOC_SCRATCH_FLOATS floats (16 MiB) that
  * the library reserves statically on every GPU that loads it, for the life of
  * the process. A call whose partials do not fit returns CSA_ERR_SCRATCH before
- * launching anything (the headline and ratio-128 workloads of this repository
- * need at most 2.6 Mi floats on a 152-SM GPU).
+ * launching anything. The need is ratio * coff * head_dim floats per row
+ * group and depends on the problem alone (the row grouping never depends on
+ * the device): the 256k-token ratio-4 headline needs 1.2 Mi floats and the
+ * ratio-128 coff-1 head_dim-512 workload 2.4 Mi; ratio 128, coff 2,
+ * head_dim 64 fits up to capacity 256 (exactly 4 Mi) and is refused from 257.
  *
- * The first call on a device looks up that array's device address (once per
- * device, with the caller's device current); make that first call before any
- * stream capture. All calls share the one array and leave their partials in
- * it: calls whose kernels overlap on the GPU (different streams, or several
- * host threads) race on it and must be serialised by the caller. Nothing in
- * the array needs clearing between calls: each call overwrites every partial
- * it reads.
+ * The first call in a CUDA context of a device looks up that array's device
+ * address (with the caller's device current) and keeps it for the context;
+ * make that first call before any stream capture. After the context is
+ * destroyed and created again (cudaDeviceReset), the next call looks the
+ * address up afresh; the array's contents do not survive the reset. All calls
+ * share the one array and leave their partials in it: calls whose kernels
+ * overlap on the GPU (different streams, or several host threads) race on it
+ * and must be serialised by the caller. Nothing in the array needs clearing
+ * between calls: each call overwrites every partial it reads.
  */
 #define CSA_NOALLOC_SCRATCH_FLOATS (4 * 1024 * 1024)
 csa_status_t csa_compress_bwd_noalloc(const void* kv, const void* score, const float* ape,

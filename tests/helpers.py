@@ -86,3 +86,44 @@ def gate_bf16(got, want, name: str, frac: float = 0.001, max_abs: float = 1.6e-2
     assert r["differing"] <= allowed, f"{name}: {r['differing']} differing > {allowed} ({r})"
     assert r["max_abs"] <= max_abs, f"{name}: max_abs {r['max_abs']} > {max_abs}"
     return r
+
+
+def strict_differing(got, want) -> int:
+    """Elements whose bf16 bits differ, NaN payloads aside (signed zeros count)."""
+    g = np.asarray(got, dtype=np.uint16)
+    w = np.asarray(want, dtype=np.uint16)
+    both_nan = np.isnan(bf16_to_f64(g)) & np.isnan(bf16_to_f64(w))
+    return int(np.count_nonzero((g != w) & ~both_nan))
+
+
+def oracle_gate(case, out=None, dkv=None, dscore=None, dape=None, exact: bool = False,
+                allowed: int = 0, label: str = ""):
+    """Gate whichever outputs are given against the oracle on the same inputs:
+    out / dkv / dscore against O32 (the bf16 gate; with `exact`, at most
+    `allowed` elements whose bits differ), dape normwise against O64 (1e-5).
+    Returns the comparison figures."""
+    p = problem(case)
+    res = {}
+    if out is not None:
+        o_out = oracle.fwd32(p, case.kv, case.score, case.ape)
+        res["out"] = gate_bf16(out, o_out, f"{label} out")
+        if exact:
+            n = strict_differing(out, o_out)
+            assert n <= allowed, f"{label} out: {n} elements differ from the oracle"
+    if dkv is not None or dscore is not None:
+        o_dkv, o_ds, _ = oracle.bwd32(p, case.kv, case.score, case.ape, case.grad_out)
+        for name, g, o in (("dkv", dkv, o_dkv), ("dscore", dscore, o_ds)):
+            if g is None:
+                continue
+            res[name] = gate_bf16(g, o, f"{label} {name}")
+            if exact:
+                n = strict_differing(g, o)
+                assert n <= allowed, f"{label} {name}: {n} elements differ from the oracle"
+    if dape is not None:
+        _, _, dape64 = oracle.bwd64(p, bf16_to_f64(case.kv), bf16_to_f64(case.score),
+                                    case.ape.astype(np.float64), bf16_to_f64(case.grad_out))
+        scale = max(float(np.max(np.abs(dape64))), 1e-30)
+        rel = float(np.max(np.abs(np.asarray(dape, dtype=np.float64) - dape64))) / scale
+        assert rel <= 1e-5, f"{label} dape: normwise rel err {rel}"
+        res["dape_rel"] = rel
+    return res

@@ -105,3 +105,50 @@ def test_reference_arm_line_carries_the_contract_keys(capsys):
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_clock_sampler_summarises_the_timed_window(monkeypatch):
+    """The NVML sampler (read-only queries from a host thread) reports the
+    median SM clock and the union of active reasons over the samples taken
+    between mark() and unmark(), with the sample counts."""
+    import time
+
+    import bench
+
+    class FakeNvml:
+        def __init__(self, *a):
+            self.n = 0
+
+        def sm_max_mhz(self):
+            return 2070
+
+        def sm_mhz(self):
+            self.n += 1
+            return 1500 if self.n < 1000 and self.phase == "warm" else 2070
+
+        def reasons(self):
+            return 0x4 if self.phase == "timed" else 0x8 * (self.phase == "after")
+
+        def power_w(self):
+            return 900.0
+
+        def close(self):
+            pass
+
+    fake = FakeNvml()
+    fake.phase = "warm"
+    monkeypatch.setattr(bench, "_Nvml", lambda *a: fake)
+    c = bench.ClockSampler(0, period_s=0.0005)
+    c.start()
+    time.sleep(0.02)
+    fake.phase = "timed"
+    c.mark()
+    time.sleep(0.03)
+    c.unmark()
+    fake.phase = "after"
+    time.sleep(0.02)
+    r = c.stop()
+    assert r["samples_timed"] >= 5 and r["samples"] > r["samples_timed"]
+    assert r["sm_mhz"] == 2070 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"]  # hw_slowdown came after the window
+    assert r["power_w_max"] == 900.0

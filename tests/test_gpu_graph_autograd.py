@@ -4,11 +4,17 @@ Both calls launch on the caller's stream with no host synchronisation and no
 compilation, so a captured forward + backward replays bit-identically to the
 eager calls (cuDNN-frontend "CSA Fused Compressor", section "CUDA graphs"),
 also after the inputs are overwritten in place. The autograd wrapper must give
-exactly the C-ABI results."""
+exactly the C-ABI results (section "High-level wrappers"). Beyond those
+self-consistency checks, every replayed and every autograd result is gated
+against the CPU oracle on the same inputs: the bf16 gate for out / dkv /
+dscore (no differing bits at all in the exact mode) and 1e-5 normwise against
+the fp64 twin for dape."""
 import numpy as np
 import pytest
 
+import oracle
 import workloads
+from helpers import oracle_gate
 
 torch = pytest.importorskip("torch")
 
@@ -21,6 +27,7 @@ def gsk():
         pytest.skip("no CUDA device")
     import gated_softmax_kv_gb300 as g
     g.build()
+    oracle.build()
     return g
 
 
@@ -66,8 +73,12 @@ def test_graph_replay_matches_eager(gsk, name, exact):
         step()
     graph.replay()
     torch.cuda.synchronize()
-    for a, b in zip(eager, [_bits(x) for x in (out, dkv, ds, dape)]):
+    first = [_bits(x) for x in (out, dkv, ds, dape)]
+    for a, b in zip(eager, first):
         assert np.array_equal(a, b)
+    oracle_gate(case, out=first[0].view(np.uint16), dkv=first[1].view(np.uint16),
+                dscore=first[2].view(np.uint16), dape=dape.cpu().numpy(),
+                exact=exact, label=f"{name} replay seed 0")
 
     # new inputs in place: the replay follows them
     other = workloads.config(name, seed=7)
@@ -77,6 +88,9 @@ def test_graph_replay_matches_eager(gsk, name, exact):
     graph.replay()
     torch.cuda.synchronize()
     replayed = [_bits(x) for x in (out, dkv, ds, dape)]
+    oracle_gate(other, out=replayed[0].view(np.uint16), dkv=replayed[1].view(np.uint16),
+                dscore=replayed[2].view(np.uint16),
+                dape=dape.cpu().numpy(), exact=exact, label=f"{name} replay seed 7")
     step()
     torch.cuda.synchronize()
     for a, b in zip(replayed, [_bits(x) for x in (out, dkv, ds, dape)]):
@@ -100,6 +114,9 @@ def test_autograd_wrapper_matches_the_c_abi(gsk, exact):
                                                case.capacity, case.ratio, case.coff, case.head_dim,
                                                t["go"], exact=exact)
     torch.cuda.synchronize()
+    oracle_gate(case, out=_bits(out.detach()).view(np.uint16), dkv=_bits(kv.grad).view(np.uint16),
+                dscore=_bits(score.grad).view(np.uint16),
+                dape=ape.grad.cpu().numpy(), exact=exact, label="autograd")
     assert np.array_equal(_bits(out.detach()), _bits(ref_out))
     assert np.array_equal(_bits(kv.grad), _bits(r_dkv))
     assert np.array_equal(_bits(score.grad), _bits(r_ds))

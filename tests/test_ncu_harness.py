@@ -16,13 +16,19 @@ LAUNCH_LOG = """==PROF== Connected to process 1 (python3)
 ==PROF== Disconnected from process 1
 """
 
-RAW = """"ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","launch__registers_per_thread"
-"","","us","Mbyte","Kbyte",""
-"0","void unnamed>::fwd_small_kernel<4, 2, 512>(FwdParams)","54.0","268.0","11000.0","124"
-"1","void unnamed>::bwd_small_kernel<4, 2, 512>(BwdParams)","96.0","285.0","222000.0","128"
-"2","unnamed>::dape_reduce_kernel(const float4 *, int, long, float4 *)","6.0","5.0","0","32"
-"3","void unnamed>::fwd_small_kernel<4, 2, 512>(FwdParams)","55.0","999.0","0","124"
+RAW = """"ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","lts__t_sectors_op_write.sum","launch__registers_per_thread"
+"","","us","Mbyte","Kbyte","sector",""
+"0","void unnamed>::fwd_small_kernel<4, 2, 512>(FwdParams)","54.0","268.0","11000.0","531250","124"
+"1","void unnamed>::bwd_small_kernel<4, 2, 512>(BwdParams)","96.0","285.0","222000.0","8387500","128"
+"2","unnamed>::dape_reduce_kernel(const float4 *, int, long, float4 *)","6.0","5.0","0","512","32"
+"3","void unnamed>::fwd_small_kernel<4, 2, 512>(FwdParams)","55.0","999.0","0","0","124"
 """
+
+
+def _only(raw, kernel):
+    """The rows of one kernel, as a single-kernel capture holds them."""
+    lines = raw.splitlines()
+    return nh.parse_raw("\n".join(lines[:2] + [ln for ln in lines[2:] if kernel in ln]))
 
 
 def test_short_names():
@@ -57,21 +63,41 @@ def test_raw_units_scale_to_bytes():
     assert "—" in nh.capture_table(k)  # metrics absent from the capture
 
 
-def test_traffic_record_uses_first_launches_and_source_hashes():
-    rec = nh.traffic_record(nh.parse_raw(RAW), 65536, "cmd")
-    # forward: the first fwd launch only; backward: bwd kernel + dape reduce
-    assert rec["csa_compress_fwd"]["dram_bytes_per_unit"] == pytest.approx((268e6 + 11e6) / 65536)
-    assert rec["csa_compress_bwd"]["dram_bytes_per_unit"] == pytest.approx(
-        (285e6 + 222e6 + 5e6) / 65536)
+def test_traffic_record_from_single_kernel_captures():
+    reports = {"fwd": _only(RAW, "fwd_small"), "bwd": _only(RAW, "bwd_small"),
+               "reduce": _only(RAW, "dape_reduce")}
+    rec = nh.traffic_record(reports, 65536, "cmd")
+    f, b = rec["csa_compress_fwd"], rec["csa_compress_bwd"]
+    # forward: the first launch only; traffic = DRAM reads + bytes stored into L2
+    assert f["dram_read_bytes_per_unit"] == pytest.approx(268e6 / 65536)
+    assert f["dram_write_bytes_per_unit"] == pytest.approx(11e6 / 65536)
+    assert f["l2_write_bytes_per_unit"] == pytest.approx(531250 * 32 / 65536)
+    assert f["dram_bytes_per_unit"] == pytest.approx((268e6 + 531250 * 32) / 65536)
+    # backward call: its kernel plus the dape reduce
+    assert b["dram_bytes_per_unit"] == pytest.approx((285e6 + 5e6 + (8387500 + 512) * 32) / 65536)
+    assert b["kernel"] == "bwd_small_kernel<4, 2, 512> + dape_reduce_kernel"
     for key in ("csa_compress_fwd", "csa_compress_bwd"):
         assert rec[key]["source_hash"] == bench.source_hash(rec[key]["sources"])
     json.dumps(rec)
 
 
-def test_traffic_record_needs_both_directions():
-    only_fwd = RAW.splitlines()[:3]
+def test_traffic_record_refuses_multi_kernel_or_missing_captures():
+    both = nh.parse_raw(RAW)  # three kernels in one capture
     with pytest.raises(ValueError):
-        nh.traffic_record(nh.parse_raw("\n".join(only_fwd)), 65536, "cmd")
+        nh.traffic_record({"fwd": both, "bwd": _only(RAW, "bwd_small"),
+                           "reduce": _only(RAW, "dape_reduce")}, 65536, "cmd")
+    with pytest.raises(ValueError):
+        nh.traffic_record({"fwd": _only(RAW, "fwd_small"), "bwd": _only(RAW, "bwd_small")},
+                          65536, "cmd")
+
+
+def test_capture_takes_one_kernel_name():
+    assert nh.single_kernel_name("bwd_small_kernel") == "bwd_small_kernel"
+    for bad in ("(fwd|bwd)_small", "fwd_small|dape_reduce", "", "bwd.*", "a b"):
+        with pytest.raises(ValueError):
+            nh.single_kernel_name(bad)
+    with pytest.raises(SystemExit):  # --kernel is required
+        nh.main(["capture"])
 
 
 def test_committed_record_covers_the_bench_keys():

@@ -1,26 +1,30 @@
-"""The allocation-free backward (csa_compress_bwd_noalloc) against the regular
-one (csa_compress_bwd).
+"""The allocation-free backward (csa_compress_bwd_noalloc), against the oracle
+and against the regular backward (csa_compress_bwd).
 
 csa_compress_bwd_noalloc serves callers that cannot allocate device memory
 while the backward runs (for example a process whose device memory all
 belongs to its own allocator from start-up, or a time-critical loop that
 must stay out of the CUDA allocator). It keeps the backward's dape partials in
-a fixed device buffer of the library instead of pool memory. This file runs
-last so that a failure here comes after every other test has run; it builds
-and uploads everything it needs, so it also passes on its own in a fresh
-process.
+a fixed device buffer of the library instead of pool memory. Its results are
+gated against the CPU oracle like every other backward (the bf16 gate for dkv
+and dscore, 1e-5 normwise against the fp64 twin for dape) and must carry the
+regular backward's bits, on two calls in a row (the second finds the first
+call's partials in the buffer). This file runs last so that a failure here
+comes after every other test has run; it builds and uploads everything it
+needs, so it also passes on its own in a fresh process.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
+import oracle
 import workloads
-from helpers import gate_bf16
+from helpers import oracle_gate
 
 torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.gpu
+
+SCRATCH_ERR = 6  # CSA_ERR_SCRATCH
 
 
 @pytest.fixture(scope="module")
@@ -29,6 +33,7 @@ def lib():
         pytest.skip("no CUDA device")
     import gated_softmax_kv_gb300 as gsk
     gsk.build()
+    oracle.build()
     return gsk
 
 
@@ -48,34 +53,72 @@ def _bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("name", ["tiny", "r4d512", "r128c1"])
-def test_noalloc_backward_matches_regular_backward_twice(lib, name):
-    case = workloads.config(name)
+def _noalloc(lib, case, t, dkv, ds, dape):
+    """One call through the C ABI; returns its status (0 = CSA_OK)."""
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.load().csa_compress_bwd_noalloc(
+        t["kv"].data_ptr(), t["score"].data_ptr(), t["ape"].data_ptr(), t["cu"].data_ptr(),
+        t["cuc"].data_ptr(), case.num_seqs, case.total_tokens, case.capacity, case.ratio,
+        case.coff, case.head_dim, t["go"].data_ptr(), dkv.data_ptr(), ds.data_ptr(),
+        dape.data_ptr(), stream)
+
+
+def _check_twice(lib, case):
     t = _upload(case)
     args = (case.capacity, case.ratio, case.coff, case.head_dim)
     ref_dkv, ref_ds, ref_dape = lib.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
                                                      *args, t["go"])
     torch.cuda.synchronize()
     ref_dkv, ref_ds, ref_dape = _bits(ref_dkv), _bits(ref_ds), ref_dape.cpu().numpy()
-    stream = torch.cuda.current_stream().cuda_stream
+    gated = None
     for call in range(2):  # the second call finds the first call's partials in the buffer
         dkv = torch.full_like(t["kv"], float("nan"))
         ds = torch.full_like(t["score"], float("nan"))
         dape = torch.full_like(t["ape"], float("nan"))
-        lib.csa_compress_bwd_noalloc_ptr(
-            t["kv"].data_ptr(), t["score"].data_ptr(), t["ape"].data_ptr(), t["cu"].data_ptr(),
-            t["cuc"].data_ptr(), case.num_seqs, case.total_tokens, *args, t["go"].data_ptr(),
-            dkv.data_ptr(), ds.data_ptr(), dape.data_ptr(), stream)
+        assert _noalloc(lib, case, t, dkv, ds, dape) == 0
         torch.cuda.synchronize()
         got_dkv, got_ds, got_dape = _bits(dkv), _bits(ds), dape.cpu().numpy()
-        gate_bf16(got_dkv, ref_dkv, f"dkv call {call}")
-        gate_bf16(got_ds, ref_ds, f"dscore call {call}")
-        rel = float(np.max(np.abs(got_dape.astype(np.float64) - ref_dape))) / \
-            max(1e-30, float(np.max(np.abs(ref_dape))))
-        assert rel <= 1e-5, f"dape call {call}: rel {rel}"
-        # same kernels and launch shape: expected to agree bit for bit
+        if gated is None:
+            gated = oracle_gate(case, dkv=got_dkv, dscore=got_ds, dape=got_dape,
+                                label=f"{case.name} no-alloc call {call}")
+        # same kernels and launch shape as the regular backward: the same bits
         assert np.array_equal(got_dkv, ref_dkv) and np.array_equal(got_ds, ref_ds)
         assert np.array_equal(got_dape.view(np.uint32), ref_dape.view(np.uint32))
+    return gated
+
+
+@pytest.mark.parametrize("name", ["tiny", "r4d512", "r128c1", "headline"])
+def test_noalloc_backward_matches_the_oracle_and_the_regular_backward_twice(lib, name):
+    print(name, _check_twice(lib, workloads.config(name)))
+
+
+def test_noalloc_scratch_limit_boundary(lib):
+    """ratio 128, coff 2, head_dim 64: one row group's partial is 16384 floats
+    and the backward takes one row group per output row up to its grid size,
+    so capacity 256 needs exactly the 4 Mi floats of the buffer (accepted, and
+    checked against the oracle) and capacity 257 needs one group more
+    (refused with CSA_ERR_SCRATCH before anything is launched: the outputs
+    keep their prefill). Real buffers on both sides."""
+    lens = [128 * 128 + 5, 128 * 128 + 64]  # 256 true rows, tails dropped
+    fits = workloads.make_case("noalloc-4mi", lens, 128, 2, 64, seed=3)
+    assert fits.capacity == 256
+    _check_twice(lib, fits)
+
+    over = workloads.make_case("noalloc-4mi+1", lens, 128, 2, 64, pad_rows=1, seed=3)
+    assert over.capacity == 257
+    t = _upload(over)
+    dkv = torch.full_like(t["kv"], float("nan"))
+    ds = torch.full_like(t["score"], float("nan"))
+    dape = torch.full_like(t["ape"], float("nan"))
+    assert _noalloc(lib, over, t, dkv, ds, dape) == SCRATCH_ERR
+    torch.cuda.synchronize()
+    assert np.all(np.isnan(dkv.float().cpu().numpy())) and np.all(np.isnan(dape.cpu().numpy()))
+    # the regular backward takes the same problem from its pool
+    r_dkv, r_ds, r_dape = lib.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
+                                               over.capacity, 128, 2, 64, t["go"])
+    torch.cuda.synchronize()
+    oracle_gate(over, dkv=_bits(r_dkv), dscore=_bits(r_ds), dape=r_dape.cpu().numpy(),
+                label="regular backward past the no-alloc limit")
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer(lib):
@@ -86,8 +129,8 @@ def test_noalloc_rejects_problems_beyond_its_buffer(lib):
     with pytest.raises(lib.CsaError) as err:
         lib.csa_compress_bwd_noalloc_ptr(fake, fake, fake, fake, fake, 1, 256, 1, 128, 2, 16392,
                                          fake, fake, fake, fake, 0)
-    assert err.value.status == 6
-    # the same call straight through the C ABI (argument types set by the wrapper above)
+    assert err.value.status == SCRATCH_ERR
+    # the same call straight through the C ABI (argument types declared by load())
     st = lib.load().csa_compress_bwd_noalloc(fake, fake, fake, fake, fake, 1, 256, 1, 128, 2, 16392,
                                              fake, fake, fake, fake, None)
-    assert st == 6
+    assert st == SCRATCH_ERR
