@@ -127,10 +127,13 @@ csa_status_t csa_compress_bwd(const void* kv, const void* score, const float* ap
  * the library reserves statically on every GPU that loads it, for the life of
  * the process. A call whose partials do not fit returns CSA_ERR_SCRATCH before
  * launching anything. The need is ratio * coff * head_dim floats per row
- * group and depends on the problem alone (the row grouping never depends on
- * the device): the 256k-token ratio-4 headline needs 1.2 Mi floats and the
- * ratio-128 coff-1 head_dim-512 workload 2.4 Mi; ratio 128, coff 2,
- * head_dim 64 fits up to capacity 256 (exactly 4 Mi) and is refused from 257.
+ * group; the row groups number at most 152 x resident blocks per SM / column
+ * tiles, so the product does not grow with head_dim, and it depends on the
+ * problem alone (the row grouping never depends on the device): 1.2 Mi
+ * floats at the 256k-token ratio-4 headline, 2.4 Mi at ratio 128 (coff 1,
+ * head_dim 512). Only a single group larger than the buffer exhausts it:
+ * ratio 128, coff 2, head_dim 16384 needs exactly 4 Mi (accepted), head_dim
+ * 16392 is refused.
  *
  * The first call in a CUDA context of a device looks up that array's device
  * address (with the caller's device current) and keeps it for the context;

@@ -93,19 +93,19 @@ def test_noalloc_backward_matches_the_oracle_and_the_regular_backward_twice(lib,
 
 
 def test_noalloc_scratch_limit_boundary(lib):
-    """ratio 128, coff 2, head_dim 64: one row group's partial is 16384 floats
-    and the backward takes one row group per output row up to its grid size,
-    so capacity 256 needs exactly the 4 Mi floats of the buffer (accepted, and
-    checked against the oracle) and capacity 257 needs one group more
-    (refused with CSA_ERR_SCRATCH before anything is launched: the outputs
-    keep their prefill). Real buffers on both sides."""
-    lens = [128 * 128 + 5, 128 * 128 + 64]  # 256 true rows, tails dropped
-    fits = workloads.make_case("noalloc-4mi", lens, 128, 2, 64, seed=3)
-    assert fits.capacity == 256
+    """The buffer's edge on real buffers: the backward caps its row groups so
+    that groups * ratio * coff * head_dim stays near 2.5 Mi floats at most,
+    except when a single group alone is larger. Ratio 128, coff 2, one output
+    row: head_dim 16384 needs exactly the 4 Mi floats of the buffer (accepted,
+    checked against the oracle and the regular backward, twice), head_dim 16392
+    needs 8192 floats more (refused with CSA_ERR_SCRATCH before anything is
+    launched: the outputs keep their NaN prefill, and the regular backward
+    takes the same problem from its pool)."""
+    fits = workloads.make_case("noalloc-4mi", [128], 128, 2, 16384, seed=3)
+    assert fits.capacity == 1 and 128 * 2 * 16384 == 4 * 1024 * 1024
     _check_twice(lib, fits)
 
-    over = workloads.make_case("noalloc-4mi+1", lens, 128, 2, 64, pad_rows=1, seed=3)
-    assert over.capacity == 257
+    over = workloads.make_case("noalloc-4mi+", [128], 128, 2, 16392, seed=3)
     t = _upload(over)
     dkv = torch.full_like(t["kv"], float("nan"))
     ds = torch.full_like(t["score"], float("nan"))
@@ -113,9 +113,8 @@ def test_noalloc_scratch_limit_boundary(lib):
     assert _noalloc(lib, over, t, dkv, ds, dape) == SCRATCH_ERR
     torch.cuda.synchronize()
     assert np.all(np.isnan(dkv.float().cpu().numpy())) and np.all(np.isnan(dape.cpu().numpy()))
-    # the regular backward takes the same problem from its pool
     r_dkv, r_ds, r_dape = lib.csa_compress_bwd(t["kv"], t["score"], t["ape"], t["cu"], t["cuc"],
-                                               over.capacity, 128, 2, 64, t["go"])
+                                               over.capacity, 128, 2, 16392, t["go"])
     torch.cuda.synchronize()
     oracle_gate(over, dkv=_bits(r_dkv), dscore=_bits(r_ds), dape=r_dape.cpu().numpy(),
                 label="regular backward past the no-alloc limit")
