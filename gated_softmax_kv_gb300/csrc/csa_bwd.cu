@@ -346,14 +346,14 @@ cudaError_t run_small(const BwdParams& b, const BwdShape& s, cudaStream_t stream
 }  // namespace
 
 cudaError_t plan_bwd(const Problem& p, BwdShape* shape) {
-  if (p.exact) return plan_bwd_exact(p, shape);
+  if (p.exact) return plan_bwd_bitwise(p, shape);
   CSA_BWD_SMALL_DISPATCH(plan_small, p, shape)
   return plan_bwd_long(p, shape);  // windows of 16 slots and more
 }
 
 cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
   const Problem& p = b.p;
-  if (p.exact) return launch_bwd_exact(b, shape, stream);
+  if (p.exact) return launch_bwd_bitwise(b, shape, stream);
   CSA_BWD_SMALL_DISPATCH(run_small, b, shape, stream)
   return launch_bwd_long(b, shape, stream);
 }

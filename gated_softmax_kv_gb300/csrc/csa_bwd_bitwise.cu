@@ -1,0 +1,517 @@
+// Bitwise backward of the CSA/HCA fused Compressor for windows of W <= 8 slots
+// (sm_103a).
+//
+// cuDNN-frontend "CSA Fused Compressor", section "Numerics": for ratios 2 and 4
+// the page's backward gives dKV / dScore bit-identical to the fp32 eager
+// reference. This kernel gives the bits of the fp32 eager-order reference of
+// this library (correctly rounded exp, e / den with IEEE division, slot-order
+// sums from +0, every product and sum rounded separately, one bf16 rounding)
+// while keeping the streaming kernel's arithmetic for almost every element.
+//
+// Per (row, column) the kernel
+//  1. runs the fast path of the default backward (exp(x) = ex2.approx(RN(x
+//     log2 e)), p = e RN(1/den), S = sum RN(dp p) in slot order);
+//  2. encloses the reference's fp32 results from it. With t_k = z_k - m the
+//     reference's exp argument (the fast path computes the same z, m, t), the
+//     fast exp is within eps(t) = (kExpC1 |t| + kExpC0) 2^-24 relative of the
+//     correctly rounded exp for t in [-kTMax, 0] (checked on every fp32 t of
+//     that range by the GPU tests). Sequential sums of W terms differ from
+//     the exact sum by at most (W - 1) 2^-24 times the sum of |terms| on either
+//     side. From these, with tau >= max |t_k| over the window's valid slots:
+//       p_ref in p [1 - rho, 1 + rho],   rho = (kExpC1 tau + K_W) 2^-24,
+//     where K_W collects the exps' weighted contribution to den (at most
+//     kExpC0 + kExpC1 (W - 1) / e, since t e^t >= -1/e and den >= 1), both
+//     sides' den rounding (2 (W - 1)), the reciprocal, product and quotient
+//     roundings (3) and the inversion of the ratio; and
+//       S_ref in [S - sigma, S + sigma], sigma = (rho + 2W 2^-24) A,
+//     with A = sum |RN(dp p)|. Each enclosure is then pushed through the
+//     reference's own monotone steps with directed rounding:
+//       dkv_ref = RN(g p_ref)        in [RN(g_a p), RN(g_b p)],
+//         g_a = RD(g - rho |g|), g_b = RU(g + rho |g|);
+//       diff_ref = RN(dp - S_ref)    in [RN(dp - S_hi), RN(dp - S_lo)] = [dl, dh],
+//       dz_ref = RN(p_ref diff_ref)  in [RN(p RD(dl - rho |dl|)), RN(p RU(dh + rho |dh|))],
+//     using that RN is monotone and p > 0 (signed zeros included: an
+//     enclosure whose two ends differ in sign fails the test below);
+//  3. accepts the fast path's bits for the column when every enclosure's two
+//     ends round to the same bf16 bits (then so does the reference's value,
+//     which lies between them) and the column is in the range the bounds
+//     cover (tau <= kTMax, so every weight is a normal number, and A finite);
+//  4. otherwise recomputes the column exactly after the fast stores of the
+//     row: the warp's failing columns are staged in shared memory and taken
+//     W / 2 lanes per column (two window slots a lane, as in the exact-mode
+//     kernels: correctly rounded exp, correctly rounded division, the
+//     reference's slot-order den and S carried lane to lane), eight columns
+//     per pass at W = 8, and the exact bf16 values overwrite the fast ones
+//     while those lines are still in L2.
+// dape sums the midpoints of the dz enclosures (deterministically, in the
+// two fixed-order levels of the default backward); zero writes and row
+// groups are those of the default small-window backward.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa_bwd_common.cuh"
+#include "csa_device.cuh"
+#include "csa_exp_cr.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCv = 4;  // columns per thread (8-byte words)
+
+// softmax_exp_fast's error envelope (csa_device.cuh, checked exhaustively by
+// the GPU tests): (kExpC1 |t| + kExpC0) 2^-24 relative for t in [-kTMax, 0]
+constexpr float kExpC0 = kFastExpC0;
+constexpr float kExpC1 = kFastExpC1;
+constexpr float kTMax = kFastExpTMax;
+constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
+
+template <int W>
+struct Bounds {
+  // rho = (kExpC1 tau + 2 kExpC0 + kExpC1 (W - 1) / e + 4) 2^-24
+  //       + 2^-23 (sum of den's partial sums) / den,
+  // every term widened by 2^-10 (second-order terms, the inversion p / p_ref
+  // -> p_ref / p and the rounding of the partial-sum ratio)
+  static constexpr float kC1u = kExpC1 * kU * 1.0009765625f;
+  static constexpr float kK0u =
+      (2.0f * kExpC0 + kExpC1 * (W - 1) * 0.36787944117144233f + 4.0f) * kU * 1.0009765625f;
+  static constexpr float k2u = 2.0f * kU * 1.0009765625f;
+  // sigma = ((rho + 2^-23) A + 2^-23 (sum of |S's partial sums|)) (1 + 2^-16)
+  static constexpr float kWiden = 1.0000152587890625f;
+};
+
+__device__ __forceinline__ void st_u16(uint16_t* p, uint16_t v) {
+  asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
+  return (uint16_t)(pack_bf16x2(x, 0.0f) & 0xFFFFu);
+}
+
+// a * b + c on two lanes rounded toward -inf (RM) or +inf (RP)
+#define CSA_FMA2_DIR(NAME, RND)                                                         \
+  __device__ __forceinline__ float2 NAME(float2 a, float2 b, float2 c) {                \
+    float2 r;                                                                           \
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" \
+        "mov.b64 c, {%6, %7};\n\tfma." RND ".f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}" \
+        : "=f"(r.x), "=f"(r.y)                                                          \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));                  \
+    return r;                                                                           \
+  }
+CSA_FMA2_DIR(fma2_rm, "rm")
+CSA_FMA2_DIR(fma2_rp, "rp")
+#undef CSA_FMA2_DIR
+
+__device__ __forceinline__ float2 abs2(float2 a) { return make_float2(fabsf(a.x), fabsf(a.y)); }
+
+// A 32-bit shared-memory read the compiler cannot replace by the register
+// that was stored there.
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];"
+               : "=r"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)));
+  return v;
+}
+
+// 8-byte asynchronous copies global -> shared (the next row's window, in
+// flight while the current row computes), one group per row and thread
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
+               :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// A warp's row, as copied in: the kv and score words (4 bf16 columns) of
+// every slot, lane-consecutive, and grad_out; then the failing columns of the
+// row as lane * 4 + column.
+template <int W>
+struct RowBuf {
+  uint2 kv[W][32];
+  uint2 sc[W][32];
+  uint2 g[32];
+  uint8_t fail[32 * kCv];
+};
+
+// blockDim = (TX, TY) with TX a multiple of 32, so that a warp lies in one
+// row; a thread owns 4 consecutive columns (8-byte words) of one row at a
+// time, rows strided by the grid. D > 0 fixes head_dim at compile time.
+template <int R, int COFF, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_bitwise_kernel(const BwdParams bp) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  constexpr int W = COFF * R;
+  constexpr int L = W / 2;   // lanes per column in the exact pass
+  constexpr int P = 32 / L;  // columns per exact pass
+  using S = Slot<R, COFF>;
+  using B = Bounds<W>;
+  const Problem& p = bp.p;
+  const int d = D > 0 ? D : p.d;
+  const int TX = blockDim.x, TY = blockDim.y;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx, nthr = TX * TY;
+  const int lane = tid & 31;
+  const int ncv = d / kCv;
+  const int cv = blockIdx.x * TX + tx;
+  const bool col_ok = cv < ncv;
+  const int64_t ld = (int64_t)COFF * d;
+  const int j0 = cv * kCv;
+  const int tile_cols = TX * kCv;
+  auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
+
+  // [W][tile_cols] APE slice (later the dape combine buffer), then two row
+  // buffers per warp (the current row and the next one, in flight)
+  extern __shared__ float sm[];
+  __shared__ float tab[2 * kExpTableSize];
+  exp_cr_table(tab);
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
+  }
+  __syncthreads();
+  const float* ape_s = sm + tx * kCv;
+  RowBuf<W>* rbs = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols) + 2 * (tid >> 5);
+
+  float dacc[W][kCv];  // sums of dz_lo + dz_hi (twice dz)
+#pragma unroll
+  for (int k = 0; k < W; ++k)
+#pragma unroll
+    for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
+
+  const uint2 zero2 = make_uint2(0u, 0u);
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t stride = (int64_t)gridDim.y * TY;
+  const uint32_t lt = (1u << lane) - 1u;
+  int hint = 0;
+
+  // The window of row `row` into `buf`: asynchronous copies of kv, score and
+  // grad_out (constants for masked slots and lanes without columns); rows
+  // that read nothing (out of bounds, past capacity) copy nothing.
+  auto fetch = [&](int64_t row, const RowInfo& info, RowBuf<W>& buf) {
+    if (!row_in_bounds<R, COFF>(info, p.T) || row >= p.C) return;
+    const int64_t off = info.base * ld + j0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(info.first, k) || !col_ok) {
+        buf.kv[k][lane] = zero2;
+        buf.sc[k][lane] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+      } else {
+        cp_async8(&buf.kv[k][lane], p.kv + off + koff(k));
+        cp_async8(&buf.sc[k][lane], p.score + off + koff(k));
+      }
+    }
+    if (col_ok) cp_async8(&buf.g[lane], bp.grad_out + row * d + j0);
+    else buf.g[lane] = zero2;
+  };
+
+  // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
+  int64_t b = (int64_t)blockIdx.y * TY + ty;
+  if (b < true_rows) fetch(b, row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
+  cp_async_commit();
+  for (int it = 0; b < true_rows; ++it, b += stride) {
+    // the row's map (rows are visited in increasing order, so the segment
+    // hint makes this one cached load), then the next row into the other
+    // buffer, last read by the previous row
+    const RowInfo cur = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    __syncwarp();
+    if (b + stride < true_rows)
+      fetch(b + stride, row_info_from(p.cu, p.cuc, p.nseq, b + stride, true_rows, R, hint),
+            rbs[(it + 1) & 1]);
+    cp_async_commit();
+    cp_async_wait<1>();  // this row's copies have landed ...
+    __syncwarp();        // ... for every lane of the warp
+    RowBuf<W>& rb = rbs[it & 1];
+    if (!row_in_bounds<R, COFF>(cur, p.T)) continue;  // violated preconditions: skip
+    const int64_t rowoff = cur.base * ld + j0;
+    uint16_t* dkv_row = bp.dkv + rowoff;
+    uint16_t* dsc_row = bp.dscore + rowoff;
+    if (b < p.C) {
+      // per column pair: z = score + ape, then in place e, then p; then the
+      // packed bf16 outputs
+      float pz[W][kCv];
+      int n = 0;  // failing columns of the row so far
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        float gg[2], slo[2], shi[2], ga[2], gb[2], rho[2];
+        bool ok[2];
+        // the pair's kv and score words, from the row buffer
+        uint32_t kw[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const float2 a = *reinterpret_cast<const float2*>(ape_s + k * tile_cols + 2 * c2);
+          const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
+          kw[k] = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
+          pz[k][2 * c2] = __fadd_rn(bf16_lo(w), a.x);
+          pz[k][2 * c2 + 1] = __fadd_rn(bf16_hi(w), a.y);
+        }
+        const uint32_t gw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.g[lane]) + c2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * c2 + h;
+          float m = pz[0][c];
+#pragma unroll
+          for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
+          // smallest logit over the valid slots (fminf skips NaN; m carries it)
+          float zmin = pz[W - 1][c];
+#pragma unroll
+          for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k) zmin = fminf(zmin, pz[k][c]);
+          if (COFF == 2 && !cur.first) {
+#pragma unroll
+            for (int k = 0; k < R; ++k) zmin = fminf(zmin, pz[k][c]);
+          }
+          const float tau = __fsub_ru(m, zmin);
+          float den = 0.0f, psd = 0.0f;  // den and the sum of its rounded partial sums
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            pz[k][c] = softmax_exp_fast(__fsub_rn(pz[k][c], m));
+            den = __fadd_rn(den, pz[k][c]);
+            if (k > 0) psd = __fadd_ru(psd, den);
+          }
+          const float y = __frcp_rn(den);
+#pragma unroll
+          for (int k = 0; k < W; ++k) pz[k][c] = __fmul_rn(pz[k][c], y);
+          const float g = bf16_at(gw, h);
+          float acc = 0.0f, aabs = 0.0f, pss = 0.0f;  // S, sum |terms|, sum |partial sums|
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const float dp = __fmul_rn(g, bf16_at(kw[k], h));
+            const float t = __fmul_rn(dp, pz[k][c]);
+            acc = __fadd_rn(acc, t);
+            aabs = __fadd_ru(aabs, fabsf(t));
+            if (k > 0) pss = __fadd_ru(pss, fabsf(acc));
+          }
+          const float r =
+              __fmaf_ru(__fmul_ru(psd, y), B::k2u, __fmaf_ru(tau, B::kC1u, B::kK0u));
+          const float sigma = __fmul_ru(
+              __fmaf_ru(__fadd_ru(r, B::k2u), aabs, __fmul_ru(B::k2u, pss)), B::kWiden);
+          gg[h] = g;
+          rho[h] = r;
+          slo[h] = __fsub_rd(acc, sigma);
+          shi[h] = __fadd_ru(acc, sigma);
+          const float ag = fabsf(g);
+          ga[h] = g == 0.0f ? g : __fmaf_rd(ag, -r, g);
+          gb[h] = g == 0.0f ? g : __fmaf_ru(ag, r, g);
+          ok[h] = tau <= kTMax && aabs <= 1.2676506e30f;  // 2^100; false for NaN
+        }
+        // the two columns' enclosures on the two-lane instructions
+        const float2 g2 = make_float2(gg[0], gg[1]);
+        const float2 ga2 = make_float2(ga[0], ga[1]), gb2 = make_float2(gb[0], gb[1]);
+        const float2 rho2 = make_float2(rho[0], rho[1]), nrho2 = make_float2(-rho[0], -rho[1]);
+        const float2 slo2 = make_float2(slo[0], slo[1]), shi2 = make_float2(shi[0], shi[1]);
+        uint32_t diff = 0;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const float2 pk = make_float2(pz[k][2 * c2], pz[k][2 * c2 + 1]);
+          // dp as two scalar products: a two-lane product may be fused into
+          // the subtraction after it, and dl / dh need the reference's dp
+          const float2 dp = make_float2(__fmul_rn(g2.x, bf16_lo(kw[k])), __fmul_rn(g2.y, bf16_hi(kw[k])));
+          const float2 dl = sub2_rn(dp, shi2), dh = sub2_rn(dp, slo2);
+          const float2 zl = mul2_rn(pk, fma2_rm(abs2(dl), nrho2, dl));
+          const float2 zh = mul2_rn(pk, fma2_rp(abs2(dh), rho2, dh));
+          const uint32_t wka = pack_bf16x2(__fmul_rn(ga2.x, pk.x), __fmul_rn(ga2.y, pk.y));
+          const uint32_t wkb = pack_bf16x2(__fmul_rn(gb2.x, pk.x), __fmul_rn(gb2.y, pk.y));
+          const uint32_t wzl = pack_bf16x2(zl.x, zl.y);
+          if (!S::masked(cur.first, k)) diff |= (wka ^ wkb) | (wzl ^ pack_bf16x2(zh.x, zh.y));
+          const float2 zs = add2_rn(zl, zh);
+          dacc[k][2 * c2] = __fadd_rn(dacc[k][2 * c2], zs.x);
+          dacc[k][2 * c2 + 1] = __fadd_rn(dacc[k][2 * c2 + 1], zs.y);
+          pz[k][2 * c2] = __uint_as_float(wka);      // dkv, columns 2 c2 and 2 c2 + 1
+          pz[k][2 * c2 + 1] = __uint_as_float(wzl);  // dscore
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const bool fail = col_ok && (((h ? diff >> 16 : diff & 0xFFFFu) != 0) || !ok[h]);
+          const uint32_t mc = __ballot_sync(0xffffffffu, fail);
+          if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + 2 * c2 + h);
+          n += __popc(mc);
+        }
+      }
+      if (col_ok) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          if (S::masked(cur.first, k)) continue;
+          st_stream8(dkv_row + koff(k), make_uint2(__float_as_uint(pz[k][0]), __float_as_uint(pz[k][2])));
+          st_stream8(dsc_row + koff(k), make_uint2(__float_as_uint(pz[k][1]), __float_as_uint(pz[k][3])));
+        }
+      }
+
+      // ---- exact pass over the warp's failing columns ----
+      if (n > 0) {
+        const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
+        const int k0 = 2 * l, k1 = 2 * l + 1;
+        const bool m0 = S::masked(cur.first, k0), m1 = S::masked(cur.first, k1);
+        __syncwarp();
+        for (int base = 0; base < n; base += P) {
+          const bool act = base + q < n;
+          const int e = rb.fail[act ? base + q : base];
+          const int lo = e >> 2, c = e & 3;  // owning lane and its column
+          const uint16_t* kv16 = reinterpret_cast<const uint16_t*>(&rb.kv[0][lo]) + c;
+          const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(&rb.sc[0][lo]) + c;
+          constexpr int kStride = 32 * 4;  // 16-bit units from one slot's words to the next
+          const float sc0 = m0 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k0 * kStride] << 16);
+          const float sc1 = m1 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k1 * kStride] << 16);
+          const float x0 = m0 ? 0.0f : __uint_as_float((uint32_t)kv16[k0 * kStride] << 16);
+          const float x1 = m1 ? 0.0f : __uint_as_float((uint32_t)kv16[k1 * kStride] << 16);
+          const float g =
+              __uint_as_float((uint32_t)(reinterpret_cast<const uint16_t*>(&rb.g[lo])[c]) << 16);
+          const int tcol = (tx - lane + lo) * kCv + c;
+          const float2 z = make_float2(__fadd_rn(sc0, sm[k0 * tile_cols + tcol]),
+                                       __fadd_rn(sc1, sm[k1 * tile_cols + tcol]));
+          float mx = max_nan(z.x, z.y);
+#pragma unroll
+          for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float2 ex = exp_cr2(sub2_rn(z, make_float2(mx, mx)), tab);
+          // den and S in slot order: every lane of the column's group gathers
+          // the W values (independent shuffles) and sums them itself
+          float den = 0.0f;
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            den = __fadd_rn(den, __shfl_sync(0xffffffffu, (k & 1) ? ex.y : ex.x, gbase + k / 2));
+          const float yd = __frcp_rn(den);
+          const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
+                                    make_float2(yd, yd));
+          const float dp0 = __fmul_rn(g, x0), dp1 = __fmul_rn(g, x1);
+          const float t0 = __fmul_rn(dp0, pw.x), t1 = __fmul_rn(dp1, pw.y);
+          float sfin = 0.0f;
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            sfin = __fadd_rn(sfin, __shfl_sync(0xffffffffu, (k & 1) ? t1 : t0, gbase + k / 2));
+          if (act) {
+            const int64_t off = rowoff + (lo - lane) * kCv + c;
+            uint16_t* dk = bp.dkv + off;
+            uint16_t* dz = bp.dscore + off;
+            if (!m0) {
+              st_u16(dk + koff(k0), bf16_bits_rn(__fmul_rn(g, pw.x)));
+              st_u16(dz + koff(k0), bf16_bits_rn(__fmul_rn(pw.x, __fsub_rn(dp0, sfin))));
+            }
+            if (!m1) {
+              st_u16(dk + koff(k1), bf16_bits_rn(__fmul_rn(g, pw.y)));
+              st_u16(dz + koff(k1), bf16_bits_rn(__fmul_rn(pw.y, __fsub_rn(dp1, sfin))));
+            }
+          }
+        }
+      }
+    } else if (col_ok) {
+      // a row past capacity has no output slot: zero gradient at its positions
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        if (S::masked(cur.first, k)) continue;
+        st_stream8(dkv_row + koff(k), zero2);
+        st_stream8(dsc_row + koff(k), zero2);
+      }
+    }
+    if (cur.last && col_ok) {
+      // the segment's last row owns its block's unread first-half columns ...
+      if (COFF == 2) {
+#pragma unroll
+        for (int t = 0; t < R; ++t) {
+          st_stream8(dkv_row + t * ld, zero2);
+          st_stream8(dsc_row + t * ld, zero2);
+        }
+      }
+      // ... and the segment's tail tokens (seqlen % ratio of them)
+      const int64_t tail_end = cur.seg_end < p.T ? cur.seg_end : p.T;
+      for (int64_t tok = cur.base + R; tok < tail_end; ++tok) {
+#pragma unroll
+        for (int h = 0; h < COFF; ++h) {
+          const int64_t off = tok * ld + h * d + j0;
+          st_stream8(bp.dkv + off, zero2);
+          st_stream8(bp.dscore + off, zero2);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  zero_orphans(bp, R);
+
+  // combine the TY thread rows in ascending order, then write this CTA's
+  // slice of the partial of row group blockIdx.y (halving the sums of the
+  // two enclosure ends: exact)
+  __syncthreads();
+  for (int t = 0; t < TY; ++t) {
+    if (ty == t && col_ok) {
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+#pragma unroll
+        for (int c = 0; c < kCv; ++c) {
+          float* s = sm + k * tile_cols + tx * kCv + c;
+          *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
+        }
+    }
+    __syncthreads();
+  }
+  float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    if (col < d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = 0.5f * sm[i];
+  }
+}
+
+template <int R, int COFF, int D>
+cudaError_t plan_bitwise_d(const Problem& p, BwdShape* s) {
+  constexpr int W = COFF * R;
+  const int ncv = p.d / kCv;
+  int tx = ncv <= 128 ? ncv : 128;
+  tx = (tx + 31) / 32 * 32;  // whole warps in a row
+  const int ty = kThreads / tx;
+  const int tiles = (ncv + tx - 1) / tx;
+  const size_t smem = sizeof(float) * W * tx * kCv + 2 * sizeof(RowBuf<W>) * (size_t)(tx * ty / 32);
+  auto kern = bwd_bitwise_kernel<R, COFF, D>;
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
+  const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
+  int64_t gy = (int64_t)kGroupingSms * occ / tiles;
+  const int64_t row_blocks = (p.C + ty - 1) / ty;
+  if (gy > row_blocks) gy = row_blocks;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  s->grid = dim3(tiles, (unsigned)gy);
+  s->block = dim3(tx, ty);
+  s->smem = smem;
+  s->groups = (int32_t)gy;
+  return cudaSuccess;
+}
+
+template <int R, int COFF>
+cudaError_t plan_bitwise_rc(const Problem& p, BwdShape* s) {
+  if (p.d == 512) return plan_bitwise_d<R, COFF, 512>(p, s);
+  if (p.d == 128) return plan_bitwise_d<R, COFF, 128>(p, s);
+  return plan_bitwise_d<R, COFF, 0>(p, s);
+}
+
+template <int R, int COFF>
+cudaError_t run_bitwise_rc(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
+  auto kern = b.p.d == 512 ? bwd_bitwise_kernel<R, COFF, 512>
+             : b.p.d == 128 ? bwd_bitwise_kernel<R, COFF, 128> : bwd_bitwise_kernel<R, COFF, 0>;
+  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
+}
+
+#define CSA_BITWISE_DISPATCH(FN, ...)               \
+  switch (p.ratio * 4 + p.coff) {                   \
+    case 2 * 4 + 1: return FN<2, 1>(__VA_ARGS__);   \
+    case 2 * 4 + 2: return FN<2, 2>(__VA_ARGS__);   \
+    case 4 * 4 + 1: return FN<4, 1>(__VA_ARGS__);   \
+    case 4 * 4 + 2: return FN<4, 2>(__VA_ARGS__);   \
+    case 8 * 4 + 1: return FN<8, 1>(__VA_ARGS__);   \
+    default: return cudaErrorInvalidValue;          \
+  }
+
+}  // namespace
+
+cudaError_t plan_bwd_bitwise(const Problem& p, BwdShape* shape) {
+  CSA_BITWISE_DISPATCH(plan_bitwise_rc, p, shape)
+}
+
+cudaError_t launch_bwd_bitwise(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
+  const Problem& p = b.p;
+  CSA_BITWISE_DISPATCH(run_bitwise_rc, b, shape, stream)
+}
+
+}  // namespace csa

@@ -75,6 +75,17 @@ __device__ __forceinline__ float softmax_exp_fast(float x) {
   return ex2_approx_ftz(__fmul_rn(x, __int_as_float(0x3fb8aa3b)));
 }
 
+// Error envelope of softmax_exp_fast used by the bitwise backward: for every
+// fp32 x in [-kFastExpTMax, 0], |softmax_exp_fast(x) / CR(exp(x)) - 1| <=
+// (kFastExpC1 |x| + kFastExpC0) 2^-24, CR the correctly rounded result. The
+// |x| term is fp32(log2 e)'s error (0.22 ulp) plus the rounding of x log2 e
+// (together at most 1.23 |x| ulp of the result); the constant covers
+// ex2.approx's own error and the correct rounding. The GPU tests check the
+// envelope on every fp32 x of the range.
+constexpr float kFastExpC0 = 3.25f;
+constexpr float kFastExpC1 = 1.25f;
+constexpr float kFastExpTMax = 60.0f;
+
 // ---- paired fp32 arithmetic --------------------------------------------------
 
 // Two independent fp32 operations in one instruction (the f32x2 forms of the

@@ -1,19 +1,17 @@
-// Exact-mode kernels of the CSA/HCA fused Compressor for sm_103a
-// (csa_compress_fwd_exact / csa_compress_bwd_exact, windows of W <= 8 slots).
+// Exact-mode forward kernel of the CSA/HCA fused Compressor for sm_103a
+// (csa_compress_fwd_exact, windows of W <= 8 slots; the exact-mode backward
+// is the bitwise kernel of csa_bwd_bitwise.cu).
 //
 // cuDNN-frontend "CSA Fused Compressor", sections "Semantics" and "Numerics":
-// the same operation as the default kernels, computed in the eager order of
-// an fp32 reference so that out, dkv and dscore carry its bits:
+// the same operation as the default forward, computed in the eager order of
+// an fp32 reference so that out carries its bits:
 //   z_k = score_k + ape_k, m = max z, e_k = exp(z_k - m) correctly rounded,
 //   den = sum e (slot order), p_k = e_k / den (IEEE),
-//   forward:  out = sum_k RN(p_k kv_k) (slot order), one bf16 rounding;
-//   backward: dp_k = g kv_k, S = sum_k RN(dp_k p_k), dscore_k = p_k (dp_k - S),
-//             dkv_k = g p_k, dape[k % ratio] += dscore_k (two fixed-order
-//             levels, as in the default backward).
+//   out = sum_k RN(p_k kv_k) (slot order), one bf16 rounding.
 //
 // The correctly rounded exp costs some 40 instructions a lane where the
-// default kernels spend two, so these kernels are bound by instruction issue,
-// not by HBM. They are shaped for that: a thread owns one column pair of one
+// default kernels spend two, so this kernel is bound by instruction issue,
+// not by HBM. It is shaped for that: a thread owns one column pair of one
 // row at a time (4-byte accesses, still one coalesced 128-byte request per
 // warp and slot), runs the pair through the two-lane fp32 instructions, keeps
 // its APE columns in registers for the whole launch and leaves the registers
@@ -22,7 +20,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "csa_bwd_common.cuh"
+#include "csa_bwd_common.cuh"  // kGroupingSms
 #include "csa_device.cuh"
 #include "csa_exp_cr.cuh"
 #include "csa_internal.h"
@@ -32,14 +30,9 @@ namespace csa {
 namespace {
 
 constexpr int kExactThreads = 256;
-// resident CTAs per SM the register allocation is sized for (measured at the
-// 256k-token ratio-4 workload: the backward at 3 spills a few registers at
-// W = 8 and is still 3% faster than at 2)
+// resident CTAs per SM the register allocation is sized for
 #ifndef CSA_EXACT_FWD_MIN_BLOCKS
 #define CSA_EXACT_FWD_MIN_BLOCKS 3
-#endif
-#ifndef CSA_EXACT_BWD_MIN_BLOCKS
-#define CSA_EXACT_BWD_MIN_BLOCKS 3
 #endif
 
 __device__ __forceinline__ uint32_t ld_stream4(const uint16_t* p) {
@@ -132,140 +125,6 @@ fwd_exact_kernel(const FwdParams f) {
   }
 }
 
-// Backward: the thread mapping of the forward. dape partials accumulate per
-// thread in registers (rows in increasing order), then the TY thread rows of
-// the CTA combine in ascending order through shared memory ([W][2 TX]) and
-// the CTA writes its columns of the partial of row group blockIdx.y.
-template <int R, int COFF, int D>
-__global__ void __launch_bounds__(kExactThreads, CSA_EXACT_BWD_MIN_BLOCKS)
-bwd_exact_kernel(const BwdParams bp) {
-  grid_dependency_wait();
-  allow_dependent_launch();
-  constexpr int W = COFF * R;
-  using S = Slot<R, COFF>;
-  const Problem& p = bp.p;
-  const int d = D > 0 ? D : p.d;
-  const int TX = blockDim.x, TY = blockDim.y;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  __shared__ float tab[2 * kExpTableSize];
-  exp_cr_table(tab);
-  __syncthreads();
-  const int jp = blockIdx.x * TX + tx;
-  const bool col_ok = jp < d / 2;
-  const int j0 = 2 * jp;
-  const int64_t ld = (int64_t)COFF * d;
-  float2 a[W], dacc[W];
-#pragma unroll
-  for (int k = 0; k < W; ++k) {
-    a[k] = col_ok ? __ldg(reinterpret_cast<const float2*>(p.ape + (int64_t)S::ape_row(k) * ld +
-                                                          S::half(k) * d + j0))
-                  : make_float2(0.0f, 0.0f);
-    dacc[k] = make_float2(0.0f, 0.0f);
-  }
-
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
-  const int64_t stride = (int64_t)gridDim.y * TY;
-  int hint = 0;
-  for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
-    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
-    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
-    const int64_t rowoff = ri.base * ld + j0;
-    uint16_t* dkv_row = bp.dkv + rowoff;
-    uint16_t* dsc_row = bp.dscore + rowoff;
-    if (b < p.C) {
-      uint32_t kvw[W], scw[W];
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) {  // kv = 0, score = -inf
-          kvw[k] = 0u;
-          scw[k] = kNegInfBf16x2;
-        } else {
-          const int64_t off = rowoff + S::tok(0, k) * ld + S::half(k) * d;
-          kvw[k] = ld_stream4(p.kv + off);
-          scw[k] = ld_stream4(p.score + off);
-        }
-      }
-      const float2 g = bf16x2_to_float2(ld_stream4(bp.grad_out + b * d + j0));
-      float2 pw[W];
-#pragma unroll
-      for (int k = 0; k < W; ++k) pw[k] = add2_rn(bf16x2_to_float2(scw[k]), a[k]);
-      exact_weights<W>(pw, tab);
-      // dp_k = g kv_k, S = sum_k RN(dp_k p_k); products scalar (they feed sums)
-      float2 dp[W];
-      float2 sum = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        dp[k] = make_float2(__fmul_rn(g.x, bf16_lo(kvw[k])), __fmul_rn(g.y, bf16_hi(kvw[k])));
-        sum = add2_rn(sum, make_float2(__fmul_rn(dp[k].x, pw[k].x), __fmul_rn(dp[k].y, pw[k].y)));
-      }
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const float2 diff = sub2_rn(dp[k], sum);
-        const float2 dz = make_float2(__fmul_rn(pw[k].x, diff.x), __fmul_rn(pw[k].y, diff.y));
-        const float2 dk = mul2_rn(g, pw[k]);
-        dacc[k] = add2_rn(dacc[k], dz);
-        if (!S::masked(ri.first, k)) {
-          const int64_t off = S::tok(0, k) * ld + S::half(k) * d;
-          st_stream4(dkv_row + off, pack_bf16x2(dk.x, dk.y));
-          st_stream4(dsc_row + off, pack_bf16x2(dz.x, dz.y));
-        }
-      }
-    } else {
-      // a row past capacity has no output slot: zero gradient at its positions
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) continue;
-        const int64_t off = S::tok(0, k) * ld + S::half(k) * d;
-        st_stream4(dkv_row + off, 0u);
-        st_stream4(dsc_row + off, 0u);
-      }
-    }
-    if (ri.last) {
-      // the segment's last row owns its block's unread first-half columns ...
-      if (COFF == 2) {
-#pragma unroll
-        for (int t = 0; t < R; ++t) {
-          st_stream4(dkv_row + t * ld, 0u);
-          st_stream4(dsc_row + t * ld, 0u);
-        }
-      }
-      // ... and the segment's tail tokens (seqlen % ratio of them)
-      const int64_t tail_end = ri.seg_end < p.T ? ri.seg_end : p.T;
-      for (int64_t tok = ri.base + R; tok < tail_end; ++tok) {
-#pragma unroll
-        for (int h = 0; h < COFF; ++h) {
-          const int64_t off = tok * ld + h * d + j0;
-          st_stream4(bp.dkv + off, 0u);
-          st_stream4(bp.dscore + off, 0u);
-        }
-      }
-    }
-  }
-
-  zero_orphans(bp, R);
-
-  extern __shared__ float sm[];  // [W][2 TX]
-  const int tile_cols = 2 * TX;
-  __syncthreads();
-  for (int t = 0; t < TY; ++t) {
-    if (ty == t && col_ok) {
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        float2* s = reinterpret_cast<float2*>(sm + k * tile_cols + 2 * tx);
-        *s = t == 0 ? dacc[k] : add2_rn(*s, dacc[k]);
-      }
-    }
-    __syncthreads();
-  }
-  float* part = bp.partial + (int64_t)blockIdx.y * (R * ld);
-  const int tid = ty * TX + tx, nthr = TX * TY;
-  for (int i = tid; i < W * tile_cols; i += nthr) {
-    const int k = i / tile_cols;
-    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
-    if (col < d) part[(int64_t)S::ape_row(k) * ld + S::half(k) * d + col] = sm[i];
-  }
-}
-
 struct ExactShape {
   int tx, ty, tiles;
 };
@@ -306,28 +165,6 @@ cudaError_t launch_fwd_exact_rc(const FwdParams& f, cudaStream_t stream) {
   return launch_fwd_exact_d<R, COFF, 0>(f, stream);
 }
 
-// the launch shape does not depend on D: every instance has the same
-// occupancy limits, and the D == 0 instance stands for all of them
-template <int R, int COFF>
-cudaError_t plan_bwd_exact_rc(const Problem& p, BwdShape* out) {
-  const ExactShape s = exact_shape(p.d);
-  const size_t smem = sizeof(float) * COFF * R * 2 * s.tx;
-  auto kern = bwd_exact_kernel<R, COFF, 0>;
-  const int64_t gy = exact_rows_grid(reinterpret_cast<const void*>(kern), s, smem, p.C);
-  out->grid = dim3(s.tiles, (unsigned)gy);
-  out->block = dim3(s.tx, s.ty);
-  out->smem = smem;
-  out->groups = (int32_t)gy;
-  return cudaSuccess;
-}
-
-template <int R, int COFF>
-cudaError_t run_bwd_exact_rc(const BwdParams& b, const BwdShape& s, cudaStream_t stream) {
-  auto kern = b.p.d == 512 ? bwd_exact_kernel<R, COFF, 512>
-             : b.p.d == 128 ? bwd_exact_kernel<R, COFF, 128> : bwd_exact_kernel<R, COFF, 0>;
-  return launch_dependent(kern, s.grid, s.block, s.smem, stream, b);
-}
-
 #define CSA_EXACT_DISPATCH(FN, ...)                 \
   switch (p.ratio * 4 + p.coff) {                   \
     case 2 * 4 + 1: return FN<2, 1>(__VA_ARGS__);   \
@@ -344,15 +181,6 @@ cudaError_t launch_fwd_exact(const FwdParams& f, cudaStream_t stream) {
   const Problem& p = f.p;
   if (p.C == 0) return cudaSuccess;
   CSA_EXACT_DISPATCH(launch_fwd_exact_rc, f, stream)
-}
-
-cudaError_t plan_bwd_exact(const Problem& p, BwdShape* shape) {
-  CSA_EXACT_DISPATCH(plan_bwd_exact_rc, p, shape)
-}
-
-cudaError_t launch_bwd_exact(const BwdParams& b, const BwdShape& shape, cudaStream_t stream) {
-  const Problem& p = b.p;
-  CSA_EXACT_DISPATCH(run_bwd_exact_rc, b, shape, stream)
 }
 
 }  // namespace csa

@@ -82,10 +82,11 @@ cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t s
 cudaError_t launch_fwd_long(const FwdParams& f, cudaStream_t stream);
 cudaError_t plan_bwd_long(const Problem& p, BwdShape* shape);
 cudaError_t launch_bwd_long(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
-// The exact mode, windows of at most 8 slots (csa_exact.cu).
+// The exact-mode forward, windows of at most 8 slots (csa_exact.cu).
 cudaError_t launch_fwd_exact(const FwdParams& f, cudaStream_t stream);
-cudaError_t plan_bwd_exact(const Problem& p, BwdShape* shape);
-cudaError_t launch_bwd_exact(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
+// The bitwise backward for windows of at most 8 slots (csa_bwd_bitwise.cu).
+cudaError_t plan_bwd_bitwise(const Problem& p, BwdShape* shape);
+cudaError_t launch_bwd_bitwise(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
 cudaError_t launch_dape_reduce(const float* partial, int32_t groups, int64_t n, float* dape,
                                cudaStream_t stream);
 

@@ -70,7 +70,45 @@ __global__ void div2_kernel(const float2* __restrict__ a, const float2* __restri
   }
 }
 
+// Largest (|fast(t) - E| / E) 2^24 - kFastExpC1 |t| over every fp32 t whose
+// encoding lies in [lo, hi] (negative numbers: -0 = 0x80000000 up to
+// -kFastExpTMax), E = exp(t) in fp64 (within 2^-52 of the exact value), as
+// the bits of a non-negative double combined with atomicMax (the order of
+// non-negative doubles is that of their encodings); NaN or an infinite ratio
+// records +inf.
+__global__ void fast_exp_envelope_kernel(uint32_t lo, uint32_t hi,
+                                         unsigned long long* __restrict__ worst) {
+  double m = 0.0;
+  const uint64_t n = (uint64_t)hi - lo + 1;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const float t = __uint_as_float((uint32_t)(lo + i));
+    const double e = exp((double)t);
+    const double r = fabs((double)csa::softmax_exp_fast(t) - e) / e * 16777216.0 -
+                     (double)csa::kFastExpC1 * fabs((double)t);
+    m = (r == r) ? fmax(m, r) : __longlong_as_double(0x7ff0000000000000LL);
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(worst, (unsigned long long)__double_as_longlong(m));
+}
+
 }  // namespace
+
+// The bitwise backward's envelope of softmax_exp_fast: the constants and the
+// measured worst case over every fp32 t in [-kFastExpTMax, 0].
+extern "C" void csa_selftest_fast_exp_constants(float* c0, float* c1, float* tmax) {
+  *c0 = csa::kFastExpC0;
+  *c1 = csa::kFastExpC1;
+  *tmax = csa::kFastExpTMax;
+}
+
+// worst: one device unsigned long long, zeroed by the caller.
+extern "C" int32_t csa_selftest_fast_exp_envelope(uint32_t lo_bits, uint32_t hi_bits,
+                                                  unsigned long long* worst, cudaStream_t stream) {
+  if (hi_bits < lo_bits) return 0;
+  fast_exp_envelope_kernel<<<152 * 8, 256, 0, stream>>>(lo_bits, hi_bits, worst);
+  return (int32_t)cudaGetLastError();
+}
 
 // div2_cr on n_pairs operand pairs (a[2i], a[2i + 1]) / (b[2i], b[2i + 1]).
 extern "C" int32_t csa_selftest_div2(const float* a, const float* b, float* q, int64_t n_pairs,

@@ -233,3 +233,31 @@ def test_exact_mode_division_is_ieee():
     bad = np.nonzero(~same)[0]
     detail = [(float(a[i]), float(b[i]), float(got[i]), float(want[i])) for i in bad[:8]]
     assert bad.size == 0, f"{bad.size} quotients differ (a, b, got, want): {detail}"
+
+
+def test_fast_exp_envelope_on_every_argument():
+    """The bitwise backward accepts the fast path's bits only inside an error
+    enclosure built on softmax_exp_fast's envelope |fast(t) / CR(t) - 1| <=
+    (C1 |t| + C0) 2^-24 for t in [-TMAX, 0] (constants from the library). Every
+    fp32 t of that range (about 1.1e9 arguments) is checked on the device
+    against exp in fp64 (within 2^-52 of the exact value): the measured
+    excess over C1 |t| must stay below C0 - 1 - 2^-20 (the 1 covers the
+    correct rounding of the reference, 2^-20 the fp64 reference's error)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_softmax_kv_gb300 import nvbuild
+    nvbuild.build()
+    lib = ctypes.CDLL(nvbuild.SELFTEST_LIB)
+    c0, c1, tmax = ctypes.c_float(), ctypes.c_float(), ctypes.c_float()
+    lib.csa_selftest_fast_exp_constants(ctypes.byref(c0), ctypes.byref(c1), ctypes.byref(tmax))
+    lib.csa_selftest_fast_exp_envelope.argtypes = [ctypes.c_uint32, ctypes.c_uint32,
+                                                   ctypes.c_void_p, ctypes.c_void_p]
+    lib.csa_selftest_fast_exp_envelope.restype = ctypes.c_int32
+    worst = torch.zeros(1, dtype=torch.int64, device="cuda")
+    hi = int(np.float32(-tmax.value).view(np.uint32))
+    assert lib.csa_selftest_fast_exp_envelope(0x80000000, hi, worst.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    w = float(worst.cpu().numpy().view(np.float64)[0])
+    print(f"envelope: C0 {c0.value}, C1 {c1.value}, TMAX {tmax.value}; worst excess over "
+          f"C1 |t| = {w:.4f} units of 2^-24")
+    assert w <= c0.value - 1.0 - 2.0 ** -20
