@@ -24,11 +24,12 @@ line without ncu and profiles only if that exits 0; ncu always gets
       the per-token bytes of the forward call (its kernel's capture) and of
       the backward call (the backward kernel's capture plus the dape reduce's)
       on the headline recipe at N tokens: DRAM reads, DRAM writes, and the
-      bytes stores wrote into L2 (lts__t_sectors_op_write.sum x 32, every one
-      of which is written back to DRAM, counted even when still dirty in L2
-      at the kernel's end), written to profiles/dram_traffic.json with a hash
-      of the kernels' sources, which bench.py uses for roofline.traffic while
-      the sources are unchanged.
+      bytes the kernels' global stores wrote (l1tex global store sectors x
+      32: every one of them is written back to DRAM, also when it is still
+      dirty in L2 at the kernel's end; local-memory spill stores and the L2's
+      own traffic between GB300's two dies are not in that count), written to
+      profiles/dram_traffic.json with a hash of the kernels' sources, which
+      bench.py uses for roofline.traffic while the sources are unchanged.
 
 The parsing functions take ncu's CSV text and need no GPU.
 """
@@ -52,8 +53,10 @@ CAPTURE_METRICS = [
     ("gpu__time_duration.sum", "duration"),
     ("dram__bytes_read.sum", "DRAM read"),
     ("dram__bytes_write.sum", "DRAM write"),
-    ("lts__t_sectors_op_write.sum", "L2 write sectors (stores)"),
-    ("lts__t_sectors_op_read.sum", "L2 read sectors"),
+    ("l1tex__t_sectors_pipe_lsu_mem_global_op_st.sum", "global store sectors"),
+    ("l1tex__t_requests_pipe_lsu_mem_local_op_st.sum", "local (spill) store requests"),
+    ("lts__t_sectors_srcunit_tex_op_read.sum", "L2 read sectors from the SMs"),
+    ("lts__t_sectors_srcunit_ltcfabric.sum", "L2 sectors between the two dies"),
     ("gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", "DRAM throughput (% of peak)"),
     ("launch__registers_per_thread", "registers / thread"),
     ("launch__occupancy_limit_registers", "blocks / SM (register limit)"),
@@ -68,8 +71,10 @@ CAPTURE_METRICS = [
     ("sm__inst_executed_pipe_xu.avg.pct_of_peak_sustained_active", "XU pipe (% of peak)"),
 ]
 
-# the L2 counters a capture adds to --set full (stores into L2, loads from L2)
-EXTRA_METRICS = "lts__t_sectors_op_write.sum,lts__t_sectors_op_read.sum"
+# counters a capture asks for by name on top of --set full: global store
+# sectors (the store audit) and the SM-originated L2 traffic
+EXTRA_METRICS = ("l1tex__t_sectors_pipe_lsu_mem_global_op_st.sum,"
+                 "lts__t_sectors_srcunit_tex_op_read.sum,lts__t_sectors_srcunit_tex_op_write.sum")
 SECTOR_BYTES = 32
 
 # the calls whose traffic the record holds: the reports (one kernel each) that
@@ -204,12 +209,13 @@ def single_kernel_name(name: str) -> str:
 
 
 def launch_bytes(vals) -> dict:
-    """DRAM reads, DRAM writes and bytes stored into L2 of one captured launch."""
+    """DRAM reads, DRAM writes and bytes of global stores of one captured launch."""
     rd = metric_value(vals, "dram__bytes_read.sum")
     wr = metric_value(vals, "dram__bytes_write.sum")
-    st = metric_value(vals, "lts__t_sectors_op_write.sum")
+    st = metric_value(vals, "l1tex__t_sectors_pipe_lsu_mem_global_op_st.sum")
     if rd is None or wr is None or st is None:
-        raise ValueError("the capture lacks dram__bytes_read/write.sum or lts__t_sectors_op_write.sum")
+        raise ValueError("the capture lacks dram__bytes_read/write.sum or "
+                         "l1tex__t_sectors_pipe_lsu_mem_global_op_st.sum")
     return {"read": rd, "dram_write": wr, "l2_write": st * SECTOR_BYTES}
 
 
@@ -218,15 +224,16 @@ def traffic_record(reports, tokens: int, command: str) -> dict:
     captures: `reports` maps "fwd", "bwd" and "reduce" to parse_raw rows of
     one kernel each (the first launch of each is used; the backward call is
     its kernel plus the dape reduce). The traffic of a call is its DRAM reads
-    plus the bytes its stores wrote into L2 (all of which reach DRAM)."""
+    plus the bytes of its global stores (all of which reach DRAM)."""
     import bench  # the source hash bench.py checks the record against
-    rec = {"note": ("per-token bytes of one launch per kernel from ncu --set full (plus "
-                    "lts__t_sectors_op_write.sum) on the headline recipe scaled to %d tokens, "
+    rec = {"note": ("per-token bytes of one launch per kernel from ncu --set full "
+                    "on the headline recipe scaled to %d tokens, "
                     "one capture per kernel; bench.py scales them to the measured launch (traffic "
                     "grows with the tokens: every token's kv and score are read once). traffic = "
-                    "DRAM reads + bytes stored into L2 (every stored byte is written back; the DRAM "
-                    "write counter misses lines still dirty in L2 when the kernel ends). Valid while "
-                    "the listed sources hash to source_hash. Command: %s" % (tokens, command))}
+                    "DRAM reads + bytes of global stores (l1tex global store sectors x 32; every "
+                    "stored byte is written back, while the DRAM write counter misses lines still "
+                    "dirty in L2 when the kernel ends). Valid while the listed sources hash to "
+                    "source_hash. Command: %s" % (tokens, command))}
     for key, spec in TRAFFIC_KERNELS.items():
         tot = {"read": 0.0, "dram_write": 0.0, "l2_write": 0.0}
         names = []

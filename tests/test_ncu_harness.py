@@ -16,7 +16,7 @@ LAUNCH_LOG = """==PROF== Connected to process 1 (python3)
 ==PROF== Disconnected from process 1
 """
 
-RAW = """"ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","lts__t_sectors_op_write.sum","launch__registers_per_thread"
+RAW = """"ID","Kernel Name","gpu__time_duration.sum","dram__bytes_read.sum","dram__bytes_write.sum","l1tex__t_sectors_pipe_lsu_mem_global_op_st.sum","launch__registers_per_thread"
 "","","us","Mbyte","Kbyte","sector",""
 "0","void unnamed>::fwd_small_kernel<4, 2, 512>(FwdParams)","54.0","268.0","11000.0","531250","124"
 "1","void unnamed>::bwd_small_kernel<4, 2, 512>(BwdParams)","96.0","285.0","222000.0","8387500","128"
@@ -68,7 +68,7 @@ def test_traffic_record_from_single_kernel_captures():
                "reduce": _only(RAW, "dape_reduce")}
     rec = nh.traffic_record(reports, 65536, "cmd")
     f, b = rec["csa_compress_fwd"], rec["csa_compress_bwd"]
-    # forward: the first launch only; traffic = DRAM reads + bytes stored into L2
+    # forward: the first launch only; traffic = DRAM reads + bytes of global stores
     assert f["dram_read_bytes_per_unit"] == pytest.approx(268e6 / 65536)
     assert f["dram_write_bytes_per_unit"] == pytest.approx(11e6 / 65536)
     assert f["l2_write_bytes_per_unit"] == pytest.approx(531250 * 32 / 65536)
