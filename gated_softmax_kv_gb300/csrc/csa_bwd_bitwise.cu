@@ -15,16 +15,21 @@
 //     reference's exp argument (the fast path computes the same z, m, t), the
 //     fast exp is within eps(t) = (kExpC1 |t| + kExpC0) 2^-24 relative of the
 //     correctly rounded exp for t in [-kTMax, 0] (checked on every fp32 t of
-//     that range by the GPU tests). Sequential sums of W terms differ from
-//     the exact sum by at most (W - 1) 2^-24 times the sum of |terms| on either
-//     side. From these, with tau >= max |t_k| over the window's valid slots:
-//       p_ref in p [1 - rho, 1 + rho],   rho = (kExpC1 tau + K_W) 2^-24,
-//     where K_W collects the exps' weighted contribution to den (at most
+//     that range by the GPU tests). A sequential sum differs from the exact
+//     sum of its terms by at most 2^-24 times the sum of its rounded partial
+//     sums, on either side. From these, with tau >= max |t_k| over the
+//     window's valid slots:
+//       p_ref in p [1 - rho, 1 + rho],
+//       rho = (kExpC1 tau + 2 kExpC0 + kExpC1 (W - 1) / e + 4) 2^-24 + 2^-23 P_den / den:
+//     the slot's own exp, the exps' weighted contribution to den (at most
 //     kExpC0 + kExpC1 (W - 1) / e, since t e^t >= -1/e and den >= 1), both
-//     sides' den rounding (2 (W - 1)), the reciprocal, product and quotient
-//     roundings (3) and the inversion of the ratio; and
-//       S_ref in [S - sigma, S + sigma], sigma = (rho + 2W 2^-24) A,
-//     with A = sum |RN(dp p)|. Each enclosure is then pushed through the
+//     sides' den rounding (P_den = the sum of den's partial sums), the
+//     reciprocal, product and quotient roundings and the inversion of the
+//     ratio; and
+//       S_ref in [S - sigma, S + sigma],
+//       sigma = (rho + 2^-23) A + 2^-23 P_S,
+//     with A = sum |RN(dp p)| and P_S the sum of |S's partial sums|. Each
+//     enclosure is then pushed through the
 //     reference's own monotone steps with directed rounding:
 //       dkv_ref = RN(g p_ref)        in [RN(g_a p), RN(g_b p)],
 //         g_a = RD(g - rho |g|), g_b = RU(g + rho |g|);
@@ -37,12 +42,13 @@
 //     which lies between them) and the column is in the range the bounds
 //     cover (tau <= kTMax, so every weight is a normal number, and A finite);
 //  4. otherwise recomputes the column exactly after the fast stores of the
-//     row: the warp's failing columns are staged in shared memory and taken
-//     W / 2 lanes per column (two window slots a lane, as in the exact-mode
-//     kernels: correctly rounded exp, correctly rounded division, the
-//     reference's slot-order den and S carried lane to lane), eight columns
-//     per pass at W = 8, and the exact bf16 values overwrite the fast ones
-//     while those lines are still in L2.
+//     row, from the row's inputs in shared memory (rows arrive there by
+//     cp.async one row ahead of their computation): the warp's failing
+//     columns are taken W / 2 lanes per column (two window slots a lane:
+//     correctly rounded exp, correctly rounded division, the reference's
+//     slot-order den and S summed by every lane of the column from gathered
+//     values), eight columns per pass at W = 8, and the exact bf16 values
+//     overwrite the fast ones while those lines are still in L2.
 // dape sums the midpoints of the dz enclosures (deterministically, in the
 // two fixed-order levels of the default backward); zero writes and row
 // groups are those of the default small-window backward.
