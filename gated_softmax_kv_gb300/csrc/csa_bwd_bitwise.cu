@@ -184,11 +184,11 @@ bwd_bitwise_kernel(const BwdParams bp) {
   const float* ape_s = sm + tx * kCv;
   RowBuf<W>* rbs = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols) + 2 * (tid >> 5);
 
-  float dacc[W][kCv];  // sums of dz_lo + dz_hi (twice dz)
+  float2 dacc[W][kCv / 2];  // sums of dz_lo + dz_hi (twice dz), per column pair
 #pragma unroll
   for (int k = 0; k < W; ++k)
 #pragma unroll
-    for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
+    for (int c2 = 0; c2 < kCv / 2; ++c2) dacc[k][c2] = make_float2(0.0f, 0.0f);
 
   const uint2 zero2 = make_uint2(0u, 0u);
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
@@ -316,17 +316,17 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const float2 pk = make_float2(pz[k][2 * c2], pz[k][2 * c2 + 1]);
           // dp as two scalar products: a two-lane product may be fused into
           // the subtraction after it, and dl / dh need the reference's dp
-          const float2 dp = make_float2(__fmul_rn(g2.x, bf16_lo(kw[k])), __fmul_rn(g2.y, bf16_hi(kw[k])));
+          const uint32_t kwk = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
+          const float2 dp = make_float2(__fmul_rn(g2.x, bf16_lo(kwk)), __fmul_rn(g2.y, bf16_hi(kwk)));
           const float2 dl = sub2_rn(dp, shi2), dh = sub2_rn(dp, slo2);
           const float2 zl = mul2_rn(pk, fma2_rm(abs2(dl), nrho2, dl));
           const float2 zh = mul2_rn(pk, fma2_rp(abs2(dh), rho2, dh));
-          const uint32_t wka = pack_bf16x2(__fmul_rn(ga2.x, pk.x), __fmul_rn(ga2.y, pk.y));
-          const uint32_t wkb = pack_bf16x2(__fmul_rn(gb2.x, pk.x), __fmul_rn(gb2.y, pk.y));
+          const float2 dka = mul2_rn(ga2, pk), dkb = mul2_rn(gb2, pk);
+          const uint32_t wka = pack_bf16x2(dka.x, dka.y);
           const uint32_t wzl = pack_bf16x2(zl.x, zl.y);
-          if (!S::masked(cur.first, k)) diff |= (wka ^ wkb) | (wzl ^ pack_bf16x2(zh.x, zh.y));
-          const float2 zs = add2_rn(zl, zh);
-          dacc[k][2 * c2] = __fadd_rn(dacc[k][2 * c2], zs.x);
-          dacc[k][2 * c2 + 1] = __fadd_rn(dacc[k][2 * c2 + 1], zs.y);
+          if (!S::masked(cur.first, k))
+            diff |= (wka ^ pack_bf16x2(dkb.x, dkb.y)) | (wzl ^ pack_bf16x2(zh.x, zh.y));
+          dacc[k][c2] = add2_rn(dacc[k][c2], add2_rn(zl, zh));
           pz[k][2 * c2] = __uint_as_float(wka);      // dkv, columns 2 c2 and 2 c2 + 1
           pz[k][2 * c2 + 1] = __uint_as_float(wzl);  // dscore
         }
@@ -446,9 +446,9 @@ bwd_bitwise_kernel(const BwdParams bp) {
 #pragma unroll
       for (int k = 0; k < W; ++k)
 #pragma unroll
-        for (int c = 0; c < kCv; ++c) {
-          float* s = sm + k * tile_cols + tx * kCv + c;
-          *s = t == 0 ? dacc[k][c] : __fadd_rn(*s, dacc[k][c]);
+        for (int c2 = 0; c2 < kCv / 2; ++c2) {
+          float2* s = reinterpret_cast<float2*>(sm + k * tile_cols + tx * kCv + 2 * c2);
+          *s = t == 0 ? dacc[k][c2] : add2_rn(*s, dacc[k][c2]);
         }
     }
     __syncthreads();
