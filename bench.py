@@ -55,8 +55,10 @@ def parse():
     ap.add_argument("--exact", action="store_true",
                     help="time the exact mode (csa_compress_fwd_exact / csa_compress_bwd_exact; "
                          "windows of at most 8 slots)")
-    ap.add_argument("--l2", choices=["auto", "flush", "warm"], default="auto",
-                    help="flush L2 before every call (auto: when kv + score fit in twice the L2)")
+    ap.add_argument("--l2", choices=["auto", "flush", "clean", "warm"], default="auto",
+                    help="flush L2 before every call (auto: when kv + score fit in twice the L2); "
+                         "clean: the flush write followed by a read of a second buffer twice the L2, "
+                         "so the call does not also write back the flush's dirty lines")
     args = ap.parse_args()
     if args.workload not in ("headline", "r4d512", "r2d128rag", "r128c1") and \
             not args.workload.startswith("pack-"):
@@ -650,12 +652,16 @@ def run_gpu(args, rank, world, local):
     # then every call is preceded by a write of a buffer twice the L2 size
     # (outside the per-call events) and the step rate is taken from the calls.
     in_bytes = kv.numel() * 2 + score.numel() * 2
-    flush = args.l2 == "flush" or (args.l2 == "auto" and in_bytes < 2 * L2_BYTES)
+    flush = args.l2 in ("flush", "clean") or (args.l2 == "auto" and in_bytes < 2 * L2_BYTES)
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
+    clean = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if args.l2 == "clean" else None
+    sink = torch.empty((), dtype=torch.int64, device=dev) if clean is not None else None
 
     def l2():
         if scrub is not None:
             scrub.fill_(0x5A5A5A5A)
+        if clean is not None:
+            torch.sum(clean, dim=0, dtype=torch.int64, out=sink)
 
     clocks = ClockSampler(local, pci_bus_id(local))
     clocks.start()
@@ -734,8 +740,9 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": (WORKLOAD if T == 262144 else f"headline recipe scaled to {T} tokens")
                    if args.workload == "headline" else args.workload, "tokens": T, "true_rows": case.true_rows, "capacity": C,
                    "ratio": r, "coff": coff, "head_dim": d, "segments": case.num_seqs,
-                   "l2": (f"L2 flushed before every call ({2 * L2_BYTES >> 20} MiB write, outside the "
-                          "per-call events); value from the summed call times") if flush else
+                   "l2": (f"L2 flushed before every call ({2 * L2_BYTES >> 20} MiB write"
+                          + (f", then a {2 * L2_BYTES >> 20} MiB read that leaves it clean" if clean is not None else "")
+                          + ", outside the per-call events); value from the summed call times") if flush else
                          (f"inputs larger than L2 (kv+score {in_bytes / 2**20:.0f} MiB per step), no flush"
                           if in_bytes >= 2 * L2_BYTES else "L2 warm between calls (--l2 warm)"),
                    "step": ("csa_compress_fwd_exact + csa_compress_bwd_exact (3 kernels)" if args.exact
