@@ -57,6 +57,7 @@
 
 #include "csa_bwd_common.cuh"
 #include "csa_device.cuh"
+#include "csa_bitwise.cuh"
 #include "csa_exp_cr.cuh"
 #include "csa_internal.h"
 
@@ -65,83 +66,7 @@ namespace csa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCv = 4;  // columns per thread (8-byte words)
-
-// softmax_exp_fast's error envelope (csa_device.cuh, checked exhaustively by
-// the GPU tests): (kExpC1 |t| + kExpC0) 2^-24 relative for t in [-kTMax, 0]
-constexpr float kExpC0 = kFastExpC0;
-constexpr float kExpC1 = kFastExpC1;
-constexpr float kTMax = kFastExpTMax;
-constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
-
-template <int W>
-struct Bounds {
-  // rho = (kExpC1 tau + 2 kExpC0 + kExpC1 (W - 1) / e + 4) 2^-24
-  //       + 2^-23 (sum of den's partial sums) / den,
-  // every term widened by 2^-10 (second-order terms, the inversion p / p_ref
-  // -> p_ref / p and the rounding of the partial-sum ratio)
-  static constexpr float kC1u = kExpC1 * kU * 1.0009765625f;
-  static constexpr float kK0u =
-      (2.0f * kExpC0 + kExpC1 * (W - 1) * 0.36787944117144233f + 4.0f) * kU * 1.0009765625f;
-  static constexpr float k2u = 2.0f * kU * 1.0009765625f;
-  // sigma = ((rho + 2^-23) A + 2^-23 (sum of |S's partial sums|)) (1 + 2^-16)
-  static constexpr float kWiden = 1.0000152587890625f;
-};
-
-__device__ __forceinline__ void st_u16(uint16_t* p, uint16_t v) {
-  asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
-  return (uint16_t)(pack_bf16x2(x, 0.0f) & 0xFFFFu);
-}
-
-// a * b + c on two lanes rounded toward -inf (RM) or +inf (RP)
-#define CSA_FMA2_DIR(NAME, RND)                                                         \
-  __device__ __forceinline__ float2 NAME(float2 a, float2 b, float2 c) {                \
-    float2 r;                                                                           \
-    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" \
-        "mov.b64 c, {%6, %7};\n\tfma." RND ".f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}" \
-        : "=f"(r.x), "=f"(r.y)                                                          \
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));                  \
-    return r;                                                                           \
-  }
-CSA_FMA2_DIR(fma2_rm, "rm")
-CSA_FMA2_DIR(fma2_rp, "rp")
-#undef CSA_FMA2_DIR
-
-__device__ __forceinline__ float2 abs2(float2 a) { return make_float2(fabsf(a.x), fabsf(a.y)); }
-
-// A 32-bit shared-memory read the compiler cannot replace by the register
-// that was stored there.
-__device__ __forceinline__ uint32_t lds_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];"
-               : "=r"(v) : "r"((uint32_t)__cvta_generic_to_shared(p)));
-  return v;
-}
-
-// 8-byte asynchronous copies global -> shared (the next row's window, in
-// flight while the current row computes), one group per row and thread
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
-               :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
-}
-
-// A warp's row, as copied in: the kv and score words (4 bf16 columns) of
-// every slot, lane-consecutive, and grad_out; then the failing columns of the
-// row as lane * 4 + column.
-template <int W>
-struct RowBuf {
-  uint2 kv[W][32];
-  uint2 sc[W][32];
-  uint2 g[32];
-  uint8_t fail[32 * kCv];
-};
+using namespace bitwise;
 
 // blockDim = (TX, TY) with TX a multiple of 32, so that a warp lies in one
 // row; a thread owns 4 consecutive columns (8-byte words) of one row at a

@@ -195,7 +195,7 @@ bool supported(int ratio, int coff) {
 
 cudaError_t launch_fwd(const FwdParams& f, cudaStream_t stream) {
   if (f.p.C == 0) return cudaSuccess;
-  if (f.p.exact) return launch_fwd_exact(f, stream);
+  if (f.p.exact) return launch_fwd_bitwise(f, stream);
   switch (f.p.ratio * 4 + f.p.coff) {
     case 2 * 4 + 1: return launch_small<2, 1>(f, stream);
     case 2 * 4 + 2: return launch_small<2, 2>(f, stream);

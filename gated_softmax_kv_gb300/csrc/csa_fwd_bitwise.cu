@@ -1,0 +1,282 @@
+// Bitwise forward of the CSA/HCA fused Compressor for windows of W <= 8 slots
+// (sm_103a): csa_compress_fwd_exact.
+//
+// cuDNN-frontend "CSA Fused Compressor", sections "Semantics" and "Numerics":
+// out carries the bits of the fp32 eager-order reference of this library --
+// z_k = score_k + ape_k, m = max z, e_k = exp(z_k - m) correctly rounded,
+// den = sum e (slot order), p_k = e_k / den (IEEE), out = sum_k RN(p_k kv_k)
+// in slot order from +0, one bf16 rounding -- while keeping the streaming
+// arithmetic for almost every output.
+//
+// Per (row, column) the kernel
+//  1. runs the fast arithmetic: e = ex2.approx(RN(x log2 e)), p = e RN(1/den)
+//     and the reference's pooled sum acc = sum RN(p_k kv_k) in slot order
+//     with those weights;
+//  2. encloses the reference's pooled sum exactly as the bitwise backward
+//     encloses its S (csa_bwd_bitwise.cu): with rho the relative bound of the
+//     weights (softmax_exp_fast's envelope, both sides' den rounding through
+//     the sum of den's partial sums, the quotient roundings),
+//       acc_ref in [acc - sigma, acc + sigma],
+//       sigma = (rho + 2^-23) A + 2^-23 P,
+//     A = sum |RN(p_k kv_k)|, P = sum of |acc's partial sums| (the kv values
+//     are the reference's own, so each term's only uncertainty is p);
+//  3. accepts bf16(acc) when RD(acc - sigma) and RU(acc + sigma) round to the
+//     same bf16 bits (then so does acc_ref, which lies between them) and the
+//     column is in the range the bounds cover (tau <= kTMax, A finite);
+//  4. otherwise recomputes the output exactly after the row's stores, from
+//     the row's inputs in shared memory: W / 2 lanes per column, two window
+//     slots a lane (correctly rounded exp, correctly rounded division, den
+//     and the pooled sum in slot order, summed by every lane of the column
+//     from gathered values), eight columns per pass at W = 8.
+// Rows arrive in a per-warp shared-memory buffer by cp.async one row ahead of
+// their computation. A row whose window leaves [0, total_tokens) (violated
+// caller preconditions) gets NaN and reads nothing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa_bitwise.cuh"
+#include "csa_device.cuh"
+#include "csa_exp_cr.cuh"
+#include "csa_internal.h"
+
+namespace csa {
+
+namespace {
+
+constexpr int kThreads = 256;
+using namespace bitwise;
+
+// blockDim = (TX, TY) with TX a multiple of 32, so that a warp lies in one
+// row; a thread owns 4 consecutive columns (8-byte words) of one row at a
+// time, rows strided by the grid. D > 0 fixes head_dim at compile time.
+template <int R, int COFF, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+fwd_bitwise_kernel(const FwdParams f) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  constexpr int W = COFF * R;
+  constexpr int L = W / 2;   // lanes per column in the exact pass
+  constexpr int P = 32 / L;  // columns per exact pass
+  using S = Slot<R, COFF>;
+  using B = Bounds<W>;
+  const Problem& p = f.p;
+  const int d = D > 0 ? D : p.d;
+  const int TX = blockDim.x, TY = blockDim.y;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * TX + tx, nthr = TX * TY;
+  const int lane = tid & 31;
+  const int ncv = d / kCv;
+  const int cv = blockIdx.x * TX + tx;
+  const bool col_ok = cv < ncv;
+  const int64_t ld = (int64_t)COFF * d;
+  const int j0 = cv * kCv;
+  const int tile_cols = TX * kCv;
+  auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
+
+  // [W][tile_cols] APE slice, then two row buffers per warp (the current row
+  // and the next one, in flight)
+  extern __shared__ float sm[];
+  __shared__ float tab[2 * kExpTableSize];
+  exp_cr_table(tab);
+  for (int i = tid; i < W * tile_cols; i += nthr) {
+    const int k = i / tile_cols;
+    const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
+    sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
+  }
+  __syncthreads();
+  const float* ape_s = sm + tx * kCv;
+  RowBuf<W>* rbs = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols) + 2 * (tid >> 5);
+
+  const uint2 zero2 = make_uint2(0u, 0u);
+  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t stride = (int64_t)gridDim.y * TY;
+  const uint32_t lt = (1u << lane) - 1u;
+  int hint = 0;
+
+  // The window of row `row` into `buf`: asynchronous copies of kv and score
+  // (constants for masked slots and lanes without columns); rows that break
+  // the preconditions copy nothing.
+  auto fetch = [&](const RowInfo& info, RowBuf<W>& buf) {
+    if (!row_in_bounds<R, COFF>(info, p.T)) return;
+    const int64_t off = info.base * ld + j0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(info.first, k) || !col_ok) {
+        buf.kv[k][lane] = zero2;
+        buf.sc[k][lane] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+      } else {
+        cp_async8(&buf.kv[k][lane], p.kv + off + koff(k));
+        cp_async8(&buf.sc[k][lane], p.score + off + koff(k));
+      }
+    }
+  };
+
+  // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
+  int64_t b = (int64_t)blockIdx.y * TY + ty;
+  if (b < p.C) fetch(row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
+  cp_async_commit();
+  for (int it = 0; b < p.C; ++it, b += stride) {
+    const RowInfo cur = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    __syncwarp();
+    if (b + stride < p.C)
+      fetch(row_info_from(p.cu, p.cuc, p.nseq, b + stride, true_rows, R, hint), rbs[(it + 1) & 1]);
+    cp_async_commit();
+    cp_async_wait<1>();  // this row's copies have landed ...
+    __syncwarp();        // ... for every lane of the warp
+    RowBuf<W>& rb = rbs[it & 1];
+    uint16_t* dst = f.out + b * d + j0;
+    if (!row_in_bounds<R, COFF>(cur, p.T)) {  // violated preconditions: NaN, no access
+      if (col_ok) st_stream8(dst, make_uint2(0x7FC07FC0u, 0x7FC07FC0u));
+      continue;
+    }
+    uint32_t ow[2];
+    int n = 0;  // failing columns of the row so far
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      float2 pz[W];
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const float2 a = *reinterpret_cast<const float2*>(ape_s + k * tile_cols + 2 * c2);
+        const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
+        pz[k] = add2_rn(make_float2(bf16_lo(w), bf16_hi(w)), a);
+      }
+      float lo[2], hi[2];
+      bool ok[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        auto Z = [&](int k) -> float& { return h ? pz[k].y : pz[k].x; };
+        float m = Z(0);
+#pragma unroll
+        for (int k = 1; k < W; ++k) m = max_nan(m, Z(k));
+        // smallest logit over the valid slots (fminf skips NaN; m carries it)
+        float zmin = Z(W - 1);
+#pragma unroll
+        for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k) zmin = fminf(zmin, Z(k));
+        if (COFF == 2 && !cur.first) {
+#pragma unroll
+          for (int k = 0; k < R; ++k) zmin = fminf(zmin, Z(k));
+        }
+        const float tau = __fsub_ru(m, zmin);
+        float den = 0.0f, psd = 0.0f;  // den and the sum of its rounded partial sums
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          Z(k) = softmax_exp_fast(__fsub_rn(Z(k), m));
+          den = __fadd_rn(den, Z(k));
+          if (k > 0) psd = __fadd_ru(psd, den);
+        }
+        const float y = __frcp_rn(den);
+        float acc = 0.0f, aabs = 0.0f, pss = 0.0f;  // pooled sum, sum |terms|, sum |partial sums|
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const uint32_t kw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
+          const float t = __fmul_rn(__fmul_rn(Z(k), y), bf16_at(kw, h));
+          acc = __fadd_rn(acc, t);
+          aabs = __fadd_ru(aabs, fabsf(t));
+          if (k > 0) pss = __fadd_ru(pss, fabsf(acc));
+        }
+        const float r = __fmaf_ru(__fmul_ru(psd, y), B::k2u, __fmaf_ru(tau, B::kC1u, B::kK0u));
+        const float sigma = __fmul_ru(
+            __fmaf_ru(__fadd_ru(r, B::k2u), aabs, __fmul_ru(B::k2u, pss)), B::kWiden);
+        lo[h] = __fsub_rd(acc, sigma);
+        hi[h] = __fadd_ru(acc, sigma);
+        ok[h] = tau <= kTMax && aabs <= 1.2676506e30f;  // 2^100; false for NaN
+      }
+      ow[c2] = pack_bf16x2(lo[0], lo[1]);
+      const uint32_t diff = ow[c2] ^ pack_bf16x2(hi[0], hi[1]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool fail = col_ok && (((h ? diff >> 16 : diff & 0xFFFFu) != 0) || !ok[h]);
+        const uint32_t mc = __ballot_sync(0xffffffffu, fail);
+        if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + 2 * c2 + h);
+        n += __popc(mc);
+      }
+    }
+    if (col_ok) st_stream8(dst, make_uint2(ow[0], ow[1]));
+
+    // ---- exact pass over the warp's failing columns ----
+    if (n > 0) {
+      const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
+      const int k0 = 2 * l, k1 = 2 * l + 1;
+      const bool m0 = S::masked(cur.first, k0), m1 = S::masked(cur.first, k1);
+      __syncwarp();
+      for (int base = 0; base < n; base += P) {
+        const bool act = base + q < n;
+        const int e = rb.fail[act ? base + q : base];
+        const int lo = e >> 2, c = e & 3;  // owning lane and its column
+        const uint16_t* kv16 = reinterpret_cast<const uint16_t*>(&rb.kv[0][lo]) + c;
+        const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(&rb.sc[0][lo]) + c;
+        constexpr int kStride = 32 * 4;  // 16-bit units from one slot's words to the next
+        const float sc0 = m0 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k0 * kStride] << 16);
+        const float sc1 = m1 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k1 * kStride] << 16);
+        const float x0 = m0 ? 0.0f : __uint_as_float((uint32_t)kv16[k0 * kStride] << 16);
+        const float x1 = m1 ? 0.0f : __uint_as_float((uint32_t)kv16[k1 * kStride] << 16);
+        const int tcol = (tx - lane + lo) * kCv + c;
+        const float2 z = make_float2(__fadd_rn(sc0, sm[k0 * tile_cols + tcol]),
+                                     __fadd_rn(sc1, sm[k1 * tile_cols + tcol]));
+        float mx = max_nan(z.x, z.y);
+#pragma unroll
+        for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float2 ex = exp_cr2(sub2_rn(z, make_float2(mx, mx)), tab);
+        // den and the pooled sum in slot order: every lane of the column's
+        // group gathers the W values (independent shuffles) and sums them
+        float den = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          den = __fadd_rn(den, __shfl_sync(0xffffffffu, (k & 1) ? ex.y : ex.x, gbase + k / 2));
+        const float yd = __frcp_rn(den);
+        const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
+                                  make_float2(yd, yd));
+        const float t0 = __fmul_rn(pw.x, x0), t1 = __fmul_rn(pw.y, x1);
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, (k & 1) ? t1 : t0, gbase + k / 2));
+        if (act && l == 0) st_u16(dst + (lo - lane) * kCv + c, bf16_bits_rn(acc));
+      }
+    }
+  }
+}
+
+template <int R, int COFF, int D>
+cudaError_t launch_bitwise_d(const FwdParams& f, cudaStream_t stream) {
+  constexpr int W = COFF * R;
+  const int ncv = f.p.d / kCv;
+  int tx = ncv <= 128 ? ncv : 128;
+  tx = (tx + 31) / 32 * 32;  // whole warps in a row
+  const int ty = kThreads / tx;
+  const int tiles = (ncv + tx - 1) / tx;
+  const size_t smem = sizeof(float) * W * tx * kCv + 2 * sizeof(RowBuf<W>) * (size_t)(tx * ty / 32);
+  auto kern = fwd_bitwise_kernel<R, COFF, D>;
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
+  const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
+  const int64_t row_blocks = (f.p.C + ty - 1) / ty;
+  int64_t gy = (int64_t)sm_count() * occ / tiles;
+  if (gy < 1) gy = 1;
+  if (gy > row_blocks) gy = row_blocks;
+  if (gy > 65535) gy = 65535;
+  return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(tx, ty), smem, stream, f);
+}
+
+template <int R, int COFF>
+cudaError_t launch_bitwise_rc(const FwdParams& f, cudaStream_t stream) {
+  if (f.p.d == 512) return launch_bitwise_d<R, COFF, 512>(f, stream);
+  if (f.p.d == 128) return launch_bitwise_d<R, COFF, 128>(f, stream);
+  return launch_bitwise_d<R, COFF, 0>(f, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bitwise(const FwdParams& f, cudaStream_t stream) {
+  const Problem& p = f.p;
+  if (p.C == 0) return cudaSuccess;
+  switch (p.ratio * 4 + p.coff) {
+    case 2 * 4 + 1: return launch_bitwise_rc<2, 1>(f, stream);
+    case 2 * 4 + 2: return launch_bitwise_rc<2, 2>(f, stream);
+    case 4 * 4 + 1: return launch_bitwise_rc<4, 1>(f, stream);
+    case 4 * 4 + 2: return launch_bitwise_rc<4, 2>(f, stream);
+    case 8 * 4 + 1: return launch_bitwise_rc<8, 1>(f, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace csa

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (csa_api.cu, csa_noalloc.cu) and the
 // kernel translation units (csa_fwd.cu, csa_fwd_long.cu, csa_bwd.cu,
-// csa_bwd_long.cu, csa_exact.cu). Not installed, not part of the ABI.
+// csa_bwd_long.cu, csa_fwd_bitwise.cu, csa_bwd_bitwise.cu). Not installed,
+// not part of the ABI.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -82,8 +83,9 @@ cudaError_t launch_bwd(const BwdParams& b, const BwdShape& shape, cudaStream_t s
 cudaError_t launch_fwd_long(const FwdParams& f, cudaStream_t stream);
 cudaError_t plan_bwd_long(const Problem& p, BwdShape* shape);
 cudaError_t launch_bwd_long(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
-// The exact-mode forward, windows of at most 8 slots (csa_exact.cu).
-cudaError_t launch_fwd_exact(const FwdParams& f, cudaStream_t stream);
+// The exact-mode (bitwise) forward, windows of at most 8 slots
+// (csa_fwd_bitwise.cu).
+cudaError_t launch_fwd_bitwise(const FwdParams& f, cudaStream_t stream);
 // The bitwise backward for windows of at most 8 slots (csa_bwd_bitwise.cu).
 cudaError_t plan_bwd_bitwise(const Problem& p, BwdShape* shape);
 cudaError_t launch_bwd_bitwise(const BwdParams& b, const BwdShape& shape, cudaStream_t stream);
