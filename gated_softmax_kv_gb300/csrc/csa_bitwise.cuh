@@ -58,6 +58,23 @@ CSA_FMA2_DIR(fma2_rm, "rm")
 CSA_FMA2_DIR(fma2_rp, "rp")
 #undef CSA_FMA2_DIR
 
+// a + b, a - b, a * b on two lanes with directed rounding. Should the
+// compiler fuse a product into a following sum, the fused result is the
+// directed rounding of the exact value, so it stays on the same side of it.
+#define CSA_OP2_DIR(NAME, OP)                                                               \
+  __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                              \
+    float2 r;                                                                               \
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" OP \
+        " d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"                                            \
+        : "=f"(r.x), "=f"(r.y)                                                              \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                          \
+    return r;                                                                               \
+  }
+CSA_OP2_DIR(add2_ru, "add.rp.f32x2")
+CSA_OP2_DIR(sub2_rd, "sub.rm.f32x2")
+CSA_OP2_DIR(mul2_ru, "mul.rp.f32x2")
+#undef CSA_OP2_DIR
+
 __device__ __forceinline__ float2 abs2(float2 a) { return make_float2(fabsf(a.x), fabsf(a.y)); }
 
 // A 32-bit shared-memory read the compiler cannot replace by the register

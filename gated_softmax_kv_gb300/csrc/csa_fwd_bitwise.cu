@@ -130,9 +130,10 @@ fwd_bitwise_kernel(const FwdParams f) {
       continue;
     }
     uint32_t ow[2];
-    int n = 0;  // failing columns of the row so far
+    uint32_t fbits = 0;  // bit 2 c2 + h: column 2 c2 + h left undecided
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
+      // the column pair (2 c2, 2 c2 + 1) in the two lanes of f32x2 values
       float2 pz[W];
 #pragma unroll
       for (int k = 0; k < W; ++k) {
@@ -140,54 +141,60 @@ fwd_bitwise_kernel(const FwdParams f) {
         const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
         pz[k] = add2_rn(make_float2(bf16_lo(w), bf16_hi(w)), a);
       }
-      float lo[2], hi[2];
-      bool ok[2];
+      float2 m = pz[0];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        auto Z = [&](int k) -> float& { return h ? pz[k].y : pz[k].x; };
-        float m = Z(0);
+      for (int k = 1; k < W; ++k) m = make_float2(max_nan(m.x, pz[k].x), max_nan(m.y, pz[k].y));
+      // smallest logit over the valid slots (fminf skips NaN; m carries it)
+      float2 zmin = pz[W - 1];
 #pragma unroll
-        for (int k = 1; k < W; ++k) m = max_nan(m, Z(k));
-        // smallest logit over the valid slots (fminf skips NaN; m carries it)
-        float zmin = Z(W - 1);
+      for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k)
+        zmin = make_float2(fminf(zmin.x, pz[k].x), fminf(zmin.y, pz[k].y));
+      if (COFF == 2 && !cur.first) {
 #pragma unroll
-        for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k) zmin = fminf(zmin, Z(k));
-        if (COFF == 2 && !cur.first) {
-#pragma unroll
-          for (int k = 0; k < R; ++k) zmin = fminf(zmin, Z(k));
-        }
-        const float tau = __fsub_ru(m, zmin);
-        float den = 0.0f, psd = 0.0f;  // den and the sum of its rounded partial sums
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          Z(k) = softmax_exp_fast(__fsub_rn(Z(k), m));
-          den = __fadd_rn(den, Z(k));
-          if (k > 0) psd = __fadd_ru(psd, den);
-        }
-        const float y = __frcp_rn(den);
-        float acc = 0.0f, aabs = 0.0f, pss = 0.0f;  // pooled sum, sum |terms|, sum |partial sums|
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const uint32_t kw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
-          const float t = __fmul_rn(__fmul_rn(Z(k), y), bf16_at(kw, h));
-          acc = __fadd_rn(acc, t);
-          aabs = __fadd_ru(aabs, fabsf(t));
-          if (k > 0) pss = __fadd_ru(pss, fabsf(acc));
-        }
-        const float r = __fmaf_ru(__fmul_ru(psd, y), B::k2u, __fmaf_ru(tau, B::kC1u, B::kK0u));
-        const float sigma = __fmul_ru(
-            __fmaf_ru(__fadd_ru(r, B::k2u), aabs, __fmul_ru(B::k2u, pss)), B::kWiden);
-        lo[h] = __fsub_rd(acc, sigma);
-        hi[h] = __fadd_ru(acc, sigma);
-        ok[h] = tau <= kTMax && aabs <= 1.2676506e30f;  // 2^100; false for NaN
+        for (int k = 0; k < R; ++k) zmin = make_float2(fminf(zmin.x, pz[k].x), fminf(zmin.y, pz[k].y));
       }
-      ow[c2] = pack_bf16x2(lo[0], lo[1]);
-      const uint32_t diff = ow[c2] ^ pack_bf16x2(hi[0], hi[1]);
+      const float2 tau = make_float2(__fsub_ru(m.x, zmin.x), __fsub_ru(m.y, zmin.y));
+      float2 den = make_float2(0.0f, 0.0f), psd = den;  // den, the sum of its rounded partial sums
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const bool fail = col_ok && (((h ? diff >> 16 : diff & 0xFFFFu) != 0) || !ok[h]);
+      for (int k = 0; k < W; ++k) {
+        pz[k] = softmax_exp_fast2(sub2_rn(pz[k], m));
+        den = add2_rn(den, pz[k]);
+        if (k > 0) psd = add2_ru(psd, den);
+      }
+      const float2 y = make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+      // pooled sum, sum |terms|, sum |partial sums|
+      float2 acc = make_float2(0.0f, 0.0f), aabs = acc, pss = acc;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const uint32_t kw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
+        const float2 t = mul2_rn(mul2_rn(pz[k], y), make_float2(bf16_lo(kw), bf16_hi(kw)));
+        acc = add2_rn(acc, t);
+        aabs = add2_ru(aabs, abs2(t));
+        if (k > 0) pss = add2_ru(pss, abs2(acc));
+      }
+      const float2 k2u = make_float2(B::k2u, B::k2u);
+      const float2 r = fma2_rp(mul2_ru(psd, y), k2u,
+                               fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kK0u, B::kK0u)));
+      const float2 sigma = mul2_ru(fma2_rp(add2_ru(r, k2u), aabs, mul2_ru(k2u, pss)),
+                                   make_float2(B::kWiden, B::kWiden));
+      const float2 lo = sub2_rd(acc, sigma), hi = add2_ru(acc, sigma);
+      ow[c2] = pack_bf16x2(lo.x, lo.y);
+      const uint32_t diff = ow[c2] ^ pack_bf16x2(hi.x, hi.y);
+      // in the range the bounds cover: tau <= kTMax, A finite (false for NaN)
+      const bool ok0 = tau.x <= kTMax && aabs.x <= 1.2676506e30f;  // 2^100
+      const bool ok1 = tau.y <= kTMax && aabs.y <= 1.2676506e30f;
+      fbits |= (uint32_t)((diff & 0xFFFFu) != 0 || !ok0) << (2 * c2);
+      fbits |= (uint32_t)((diff >> 16) != 0 || !ok1) << (2 * c2 + 1);
+    }
+    if (!col_ok) fbits = 0;
+    // the warp's undecided columns, as lane * 4 + column, in rb.fail[0, n)
+    int n = 0;
+    if (__any_sync(0xffffffffu, fbits != 0)) {
+#pragma unroll
+      for (int i = 0; i < kCv; ++i) {
+        const bool fail = (fbits >> i) & 1u;
         const uint32_t mc = __ballot_sync(0xffffffffu, fail);
-        if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + 2 * c2 + h);
+        if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + i);
         n += __popc(mc);
       }
     }
