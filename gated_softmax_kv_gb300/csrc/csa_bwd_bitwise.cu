@@ -32,7 +32,8 @@
 //     enclosure is then pushed through the
 //     reference's own monotone steps with directed rounding:
 //       dkv_ref = RN(g p_ref)        in [RN(g_a p), RN(g_b p)],
-//         g_a = RD(g - rho |g|), g_b = RU(g + rho |g|);
+//         g_a = RD(g - rho |g|), g_b = RU(g + rho |g|), each given the sign
+//         of g (so that g = +0 or -0 gives its own zero at both ends);
 //       diff_ref = RN(dp - S_ref)    in [RN(dp - S_hi), RN(dp - S_lo)] = [dl, dh],
 //       dz_ref = RN(p_ref diff_ref)  in [RN(p RD(dl - rho |dl|)), RN(p RU(dh + rho |dh|))],
 //     using that RN is monotone and p > 0 (signed zeros included: an
@@ -163,14 +164,12 @@ bwd_bitwise_kernel(const BwdParams bp) {
     uint16_t* dkv_row = bp.dkv + rowoff;
     uint16_t* dsc_row = bp.dscore + rowoff;
     if (b < p.C) {
-      // per column pair: z = score + ape, then in place e, then p; then the
-      // packed bf16 outputs
-      float pz[W][kCv];
+      // per column pair (the two lanes of f32x2 values): z = score + ape,
+      // then in place e, then p; then the packed bf16 outputs
+      float2 pz[W][2];
       int n = 0;  // failing columns of the row so far
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        float gg[2], slo[2], shi[2], ga[2], gb[2], rho[2];
-        bool ok[2];
         // the pair's kv and score words, from the row buffer
         uint32_t kw[W];
 #pragma unroll
@@ -178,67 +177,63 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const float2 a = *reinterpret_cast<const float2*>(ape_s + k * tile_cols + 2 * c2);
           const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
           kw[k] = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
-          pz[k][2 * c2] = __fadd_rn(bf16_lo(w), a.x);
-          pz[k][2 * c2 + 1] = __fadd_rn(bf16_hi(w), a.y);
+          pz[k][c2] = add2_rn(make_float2(bf16_lo(w), bf16_hi(w)), a);
         }
         const uint32_t gw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.g[lane]) + c2);
+        float2 m = pz[0][c2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * c2 + h;
-          float m = pz[0][c];
+        for (int k = 1; k < W; ++k) m = make_float2(max_nan(m.x, pz[k][c2].x), max_nan(m.y, pz[k][c2].y));
+        // smallest logit over the valid slots (fminf skips NaN; m carries it)
+        float2 zmin = pz[W - 1][c2];
 #pragma unroll
-          for (int k = 1; k < W; ++k) m = max_nan(m, pz[k][c]);
-          // smallest logit over the valid slots (fminf skips NaN; m carries it)
-          float zmin = pz[W - 1][c];
+        for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k)
+          zmin = make_float2(fminf(zmin.x, pz[k][c2].x), fminf(zmin.y, pz[k][c2].y));
+        if (COFF == 2 && !cur.first) {
 #pragma unroll
-          for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k) zmin = fminf(zmin, pz[k][c]);
-          if (COFF == 2 && !cur.first) {
-#pragma unroll
-            for (int k = 0; k < R; ++k) zmin = fminf(zmin, pz[k][c]);
-          }
-          const float tau = __fsub_ru(m, zmin);
-          float den = 0.0f, psd = 0.0f;  // den and the sum of its rounded partial sums
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            pz[k][c] = softmax_exp_fast(__fsub_rn(pz[k][c], m));
-            den = __fadd_rn(den, pz[k][c]);
-            if (k > 0) psd = __fadd_ru(psd, den);
-          }
-          const float y = __frcp_rn(den);
-#pragma unroll
-          for (int k = 0; k < W; ++k) pz[k][c] = __fmul_rn(pz[k][c], y);
-          const float g = bf16_at(gw, h);
-          float acc = 0.0f, aabs = 0.0f, pss = 0.0f;  // S, sum |terms|, sum |partial sums|
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const float dp = __fmul_rn(g, bf16_at(kw[k], h));
-            const float t = __fmul_rn(dp, pz[k][c]);
-            acc = __fadd_rn(acc, t);
-            aabs = __fadd_ru(aabs, fabsf(t));
-            if (k > 0) pss = __fadd_ru(pss, fabsf(acc));
-          }
-          const float r =
-              __fmaf_ru(__fmul_ru(psd, y), B::k2u, __fmaf_ru(tau, B::kC1u, B::kK0u));
-          const float sigma = __fmul_ru(
-              __fmaf_ru(__fadd_ru(r, B::k2u), aabs, __fmul_ru(B::k2u, pss)), B::kWiden);
-          gg[h] = g;
-          rho[h] = r;
-          slo[h] = __fsub_rd(acc, sigma);
-          shi[h] = __fadd_ru(acc, sigma);
-          const float ag = fabsf(g);
-          ga[h] = g == 0.0f ? g : __fmaf_rd(ag, -r, g);
-          gb[h] = g == 0.0f ? g : __fmaf_ru(ag, r, g);
-          ok[h] = tau <= kTMax && aabs <= 1.2676506e30f;  // 2^100; false for NaN
+          for (int k = 0; k < R; ++k)
+            zmin = make_float2(fminf(zmin.x, pz[k][c2].x), fminf(zmin.y, pz[k][c2].y));
         }
-        // the two columns' enclosures on the two-lane instructions
-        const float2 g2 = make_float2(gg[0], gg[1]);
-        const float2 ga2 = make_float2(ga[0], ga[1]), gb2 = make_float2(gb[0], gb[1]);
-        const float2 rho2 = make_float2(rho[0], rho[1]), nrho2 = make_float2(-rho[0], -rho[1]);
-        const float2 slo2 = make_float2(slo[0], slo[1]), shi2 = make_float2(shi[0], shi[1]);
+        const float2 tau = make_float2(__fsub_ru(m.x, zmin.x), __fsub_ru(m.y, zmin.y));
+        float2 den = make_float2(0.0f, 0.0f), psd = den;  // den, the sum of its rounded partial sums
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          pz[k][c2] = softmax_exp_fast2(sub2_rn(pz[k][c2], m));
+          den = add2_rn(den, pz[k][c2]);
+          if (k > 0) psd = add2_ru(psd, den);
+        }
+        const float2 y = make_float2(__frcp_rn(den.x), __frcp_rn(den.y));
+#pragma unroll
+        for (int k = 0; k < W; ++k) pz[k][c2] = mul2_rn(pz[k][c2], y);
+        const float2 g2 = make_float2(bf16_lo(gw), bf16_hi(gw));
+        // S, sum |terms|, sum |partial sums|
+        float2 acc = make_float2(0.0f, 0.0f), aabs = acc, pss = acc;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const float2 dp = mul2_rn(g2, make_float2(bf16_lo(kw[k]), bf16_hi(kw[k])));
+          const float2 t = mul2_rn(dp, pz[k][c2]);
+          acc = add2_rn(acc, t);
+          aabs = add2_ru(aabs, abs2(t));
+          if (k > 0) pss = add2_ru(pss, abs2(acc));
+        }
+        const float2 k2u = make_float2(B::k2u, B::k2u);
+        const float2 rho2 = fma2_rp(mul2_ru(psd, y), k2u,
+                                    fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kK0u, B::kK0u)));
+        const float2 nrho2 = make_float2(-rho2.x, -rho2.y);
+        const float2 sigma = mul2_ru(fma2_rp(add2_ru(rho2, k2u), aabs, mul2_ru(k2u, pss)),
+                                     make_float2(B::kWiden, B::kWiden));
+        const float2 slo2 = sub2_rd(acc, sigma), shi2 = add2_ru(acc, sigma);
+        // g -/+ rho |g| rounded outwards, with the sign of g: the directed
+        // roundings give -0 / +0 at g = +0 / -0, and g p_ref has g's sign
+        const float2 ga = fma2_rm(abs2(g2), nrho2, g2), gb = fma2_rp(abs2(g2), rho2, g2);
+        const float2 ga2 = make_float2(copysignf(ga.x, g2.x), copysignf(ga.y, g2.y));
+        const float2 gb2 = make_float2(copysignf(gb.x, g2.x), copysignf(gb.y, g2.y));
+        // in the range the bounds cover: tau <= kTMax, A finite (false for NaN)
+        const bool ok0 = tau.x <= kTMax && aabs.x <= 1.2676506e30f;  // 2^100
+        const bool ok1 = tau.y <= kTMax && aabs.y <= 1.2676506e30f;
         uint32_t diff = 0;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          const float2 pk = make_float2(pz[k][2 * c2], pz[k][2 * c2 + 1]);
+          const float2 pk = pz[k][c2];
           // dp as two scalar products: a two-lane product may be fused into
           // the subtraction after it, and dl / dh need the reference's dp
           const uint32_t kwk = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
@@ -252,12 +247,12 @@ bwd_bitwise_kernel(const BwdParams bp) {
           if (!S::masked(cur.first, k))
             diff |= (wka ^ pack_bf16x2(dkb.x, dkb.y)) | (wzl ^ pack_bf16x2(zh.x, zh.y));
           dacc[k][c2] = add2_rn(dacc[k][c2], add2_rn(zl, zh));
-          pz[k][2 * c2] = __uint_as_float(wka);      // dkv, columns 2 c2 and 2 c2 + 1
-          pz[k][2 * c2 + 1] = __uint_as_float(wzl);  // dscore
+          // dkv and dscore words of columns 2 c2 and 2 c2 + 1
+          pz[k][c2] = make_float2(__uint_as_float(wka), __uint_as_float(wzl));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const bool fail = col_ok && (((h ? diff >> 16 : diff & 0xFFFFu) != 0) || !ok[h]);
+          const bool fail = col_ok && (((h ? diff >> 16 : diff & 0xFFFFu) != 0) || !(h ? ok1 : ok0));
           const uint32_t mc = __ballot_sync(0xffffffffu, fail);
           if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + 2 * c2 + h);
           n += __popc(mc);
@@ -267,8 +262,8 @@ bwd_bitwise_kernel(const BwdParams bp) {
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           if (S::masked(cur.first, k)) continue;
-          st_stream8(dkv_row + koff(k), make_uint2(__float_as_uint(pz[k][0]), __float_as_uint(pz[k][2])));
-          st_stream8(dsc_row + koff(k), make_uint2(__float_as_uint(pz[k][1]), __float_as_uint(pz[k][3])));
+          st_stream8(dkv_row + koff(k), make_uint2(__float_as_uint(pz[k][0].x), __float_as_uint(pz[k][1].x)));
+          st_stream8(dsc_row + koff(k), make_uint2(__float_as_uint(pz[k][0].y), __float_as_uint(pz[k][1].y)));
         }
       }
 
