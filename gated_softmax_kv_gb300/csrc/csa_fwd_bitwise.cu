@@ -23,11 +23,15 @@
 //  3. accepts bf16(acc) when RD(acc - sigma) and RU(acc + sigma) round to the
 //     same bf16 bits (then so does acc_ref, which lies between them) and the
 //     column is in the range the bounds cover (tau <= kTMax, A finite);
-//  4. otherwise recomputes the output exactly after the row's stores, from
-//     the row's inputs in shared memory: W / 2 lanes per column, two window
-//     slots a lane (correctly rounded exp, correctly rounded division, den
-//     and the pooled sum in slot order, summed by every lane of the column
-//     from gathered values), eight columns per pass at W = 8.
+//  4. otherwise queues the column (its window copied out of the row buffer,
+//     its output offset) in a per-warp shared-memory queue of 64 / W
+//     columns. A full queue, and at the end what is left in it, takes one
+//     exact pass that overwrites the fast outputs: W / 2 lanes per column,
+//     two window slots a lane (correctly rounded exp, correctly rounded
+//     division, den and the pooled sum in slot order, summed by every lane
+//     of the column from gathered values). About 0.5% of the columns fail
+//     at the headline, so a pass comes every ~12 rows of a warp instead of a
+//     nearly empty one in half the rows.
 // Rows arrive in a per-warp shared-memory buffer by cp.async one row ahead of
 // their computation. A row whose window leaves [0, total_tokens) (violated
 // caller preconditions) gets NaN and reads nothing.
@@ -74,7 +78,7 @@ fwd_bitwise_kernel(const FwdParams f) {
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
   // [W][tile_cols] APE slice, then two row buffers per warp (the current row
-  // and the next one, in flight)
+  // and the next one, in flight), then the warps' queues of undecided columns
   extern __shared__ float sm[];
   __shared__ float tab[2 * kExpTableSize];
   exp_cr_table(tab);
@@ -85,7 +89,11 @@ fwd_bitwise_kernel(const FwdParams f) {
   }
   __syncthreads();
   const float* ape_s = sm + tx * kCv;
-  RowBuf<W>* rbs = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols) + 2 * (tid >> 5);
+  RowBuf<W>* const rb0 = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols);
+  RowBuf<W>* rbs = rb0 + 2 * (tid >> 5);
+  Pending<W>& pq = reinterpret_cast<Pending<W>*>(rb0 + 2 * (nthr >> 5))[tid >> 5];
+  constexpr int kCap = Pending<W>::kCap;
+  static_assert(kCap == P, "a pass takes the whole queue");
 
   const uint2 zero2 = make_uint2(0u, 0u);
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
@@ -110,6 +118,41 @@ fwd_bitwise_kernel(const FwdParams f) {
       }
     }
   };
+
+  // The exact pass over the first cnt queued columns: W / 2 lanes a column,
+  // two window slots a lane (correctly rounded exp and division), den and the
+  // pooled sum in slot order, summed by every lane of the column's group
+  // from gathered values (independent shuffles).
+  auto exact_pass = [&](int cnt) {
+    const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
+    __syncwarp();
+    const bool act = q < cnt;
+    const int qe = act ? q : 0;
+    const uint32_t sw = lds_u32(&pq.sc[qe][2 * l]);  // slots 2 l and 2 l + 1
+    const uint32_t kw = lds_u32(&pq.kv[qe][2 * l]);
+    const int tcol = pq.tcol[qe];
+    const float2 z = make_float2(__fadd_rn(bf16_lo(sw), sm[(2 * l) * tile_cols + tcol]),
+                                 __fadd_rn(bf16_hi(sw), sm[(2 * l + 1) * tile_cols + tcol]));
+    float mx = max_nan(z.x, z.y);
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float2 ex = exp_cr2(sub2_rn(z, make_float2(mx, mx)), tab);
+    float den = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      den = __fadd_rn(den, __shfl_sync(0xffffffffu, (k & 1) ? ex.y : ex.x, gbase + k / 2));
+    const float yd = __frcp_rn(den);
+    const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
+                              make_float2(yd, yd));
+    const float t0 = __fmul_rn(pw.x, bf16_lo(kw)), t1 = __fmul_rn(pw.y, bf16_hi(kw));
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, (k & 1) ? t1 : t0, gbase + k / 2));
+    if (act && l == 0) st_u16(f.out + pq.off[qe], bf16_bits_rn(acc));
+    __syncwarp();
+  };
+  int pend = 0;  // queued columns
 
   // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
   int64_t b = (int64_t)blockIdx.y * TY + ty;
@@ -200,48 +243,32 @@ fwd_bitwise_kernel(const FwdParams f) {
     }
     if (col_ok) st_stream8(dst, make_uint2(ow[0], ow[1]));
 
-    // ---- exact pass over the warp's failing columns ----
-    if (n > 0) {
-      const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
-      const int k0 = 2 * l, k1 = 2 * l + 1;
-      const bool m0 = S::masked(cur.first, k0), m1 = S::masked(cur.first, k1);
+    // queue the row's undecided columns; a full queue takes one exact pass
+    for (int i = 0; i < n;) {
+      const int take = min(n - i, kCap - pend);
       __syncwarp();
-      for (int base = 0; base < n; base += P) {
-        const bool act = base + q < n;
-        const int e = rb.fail[act ? base + q : base];
+      for (int j = lane; j < take * W; j += 32) {
+        const int en = j / W, k = j % W;
+        const int e = rb.fail[i + en];
         const int lo = e >> 2, c = e & 3;  // owning lane and its column
-        const uint16_t* kv16 = reinterpret_cast<const uint16_t*>(&rb.kv[0][lo]) + c;
-        const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(&rb.sc[0][lo]) + c;
-        constexpr int kStride = 32 * 4;  // 16-bit units from one slot's words to the next
-        const float sc0 = m0 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k0 * kStride] << 16);
-        const float sc1 = m1 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k1 * kStride] << 16);
-        const float x0 = m0 ? 0.0f : __uint_as_float((uint32_t)kv16[k0 * kStride] << 16);
-        const float x1 = m1 ? 0.0f : __uint_as_float((uint32_t)kv16[k1 * kStride] << 16);
-        const int tcol = (tx - lane + lo) * kCv + c;
-        const float2 z = make_float2(__fadd_rn(sc0, sm[k0 * tile_cols + tcol]),
-                                     __fadd_rn(sc1, sm[k1 * tile_cols + tcol]));
-        float mx = max_nan(z.x, z.y);
-#pragma unroll
-        for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float2 ex = exp_cr2(sub2_rn(z, make_float2(mx, mx)), tab);
-        // den and the pooled sum in slot order: every lane of the column's
-        // group gathers the W values (independent shuffles) and sums them
-        float den = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k)
-          den = __fadd_rn(den, __shfl_sync(0xffffffffu, (k & 1) ? ex.y : ex.x, gbase + k / 2));
-        const float yd = __frcp_rn(den);
-        const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
-                                  make_float2(yd, yd));
-        const float t0 = __fmul_rn(pw.x, x0), t1 = __fmul_rn(pw.y, x1);
-        float acc = 0.0f;
-#pragma unroll
-        for (int k = 0; k < W; ++k)
-          acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, (k & 1) ? t1 : t0, gbase + k / 2));
-        if (act && l == 0) st_u16(dst + (lo - lane) * kCv + c, bf16_bits_rn(acc));
+        pq.sc[pend + en][k] = reinterpret_cast<const uint16_t*>(&rb.sc[k][lo])[c];
+        pq.kv[pend + en][k] = reinterpret_cast<const uint16_t*>(&rb.kv[k][lo])[c];
+      }
+      if (lane < take) {
+        const int e = rb.fail[i + lane];
+        const int lo = e >> 2, c = e & 3;
+        pq.tcol[pend + lane] = (uint16_t)((tx - lane + lo) * kCv + c);
+        pq.off[pend + lane] = b * d + j0 + (lo - lane) * kCv + c;
+      }
+      pend += take;
+      i += take;
+      if (pend == kCap) {
+        exact_pass(kCap);
+        pend = 0;
       }
     }
   }
+  if (pend > 0) exact_pass(pend);
 }
 
 template <int R, int COFF, int D>
@@ -252,7 +279,8 @@ cudaError_t launch_bitwise_d(const FwdParams& f, cudaStream_t stream) {
   tx = (tx + 31) / 32 * 32;  // whole warps in a row
   const int ty = kThreads / tx;
   const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kCv + 2 * sizeof(RowBuf<W>) * (size_t)(tx * ty / 32);
+  const size_t smem = sizeof(float) * W * tx * kCv +
+                      (2 * sizeof(RowBuf<W>) + sizeof(Pending<W>)) * (size_t)(tx * ty / 32);
   auto kern = fwd_bitwise_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
