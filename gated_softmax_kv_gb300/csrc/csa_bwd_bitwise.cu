@@ -177,22 +177,22 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const float2 a = *reinterpret_cast<const float2*>(ape_s + k * tile_cols + 2 * c2);
           const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
           kw[k] = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
-          pz[k][c2] = add2_rn(make_float2(bf16_lo(w), bf16_hi(w)), a);
+          uint16_t s0, s1;
+          split_bf16x2(w, s0, s1);
+          pz[k][c2] = make_float2(add_bf16_f32(s0, a.x), add_bf16_f32(s1, a.y));
         }
         const uint32_t gw = lds_u32(reinterpret_cast<const uint32_t*>(&rb.g[lane]) + c2);
-        float2 m = pz[0][c2];
-#pragma unroll
-        for (int k = 1; k < W; ++k) m = make_float2(max_nan(m.x, pz[k][c2].x), max_nan(m.y, pz[k][c2].y));
+        uint16_t g0, g1;
+        split_bf16x2(gw, g0, g1);
+        auto zx = [&](int k) { return pz[k][c2].x; };
+        auto zy = [&](int k) { return pz[k][c2].y; };
+        const float2 m = make_float2(max_range<0, W>(zx), max_range<0, W>(zy));
         // smallest logit over the valid slots (fminf skips NaN; m carries it)
-        float2 zmin = pz[W - 1][c2];
-#pragma unroll
-        for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k)
-          zmin = make_float2(fminf(zmin.x, pz[k][c2].x), fminf(zmin.y, pz[k][c2].y));
-        if (COFF == 2 && !cur.first) {
-#pragma unroll
-          for (int k = 0; k < R; ++k)
-            zmin = make_float2(fminf(zmin.x, pz[k][c2].x), fminf(zmin.y, pz[k][c2].y));
-        }
+        constexpr int kLoValid = COFF == 2 ? R : 0;  // first slot valid on every row
+        float2 zmin = make_float2(min_range<kLoValid, W>(zx), min_range<kLoValid, W>(zy));
+        if (COFF == 2 && !cur.first)
+          zmin = make_float2(fminf(zmin.x, min_range<0, (COFF == 2 ? R : 1)>(zx)),
+                             fminf(zmin.y, min_range<0, (COFF == 2 ? R : 1)>(zy)));
         const float2 tau = make_float2(__fsub_ru(m.x, zmin.x), __fsub_ru(m.y, zmin.y));
         float2 den = make_float2(0.0f, 0.0f), psd = den;  // den, the sum of its rounded partial sums
 #pragma unroll
@@ -209,7 +209,9 @@ bwd_bitwise_kernel(const BwdParams bp) {
         float2 acc = make_float2(0.0f, 0.0f), aabs = acc, pss = acc;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          const float2 dp = mul2_rn(g2, make_float2(bf16_lo(kw[k]), bf16_hi(kw[k])));
+          uint16_t v0, v1;
+          split_bf16x2(kw[k], v0, v1);
+          const float2 dp = make_float2(mul_bf16(g0, v0), mul_bf16(g1, v1));  // RN(g kv)
           const float2 t = mul2_rn(dp, pz[k][c2]);
           acc = add2_rn(acc, t);
           aabs = add2_ru(aabs, abs2(t));
@@ -234,10 +236,12 @@ bwd_bitwise_kernel(const BwdParams bp) {
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           const float2 pk = pz[k][c2];
-          // dp as two scalar products: a two-lane product may be fused into
-          // the subtraction after it, and dl / dh need the reference's dp
+          // the reference's dp = RN(g kv) as bf16 FMAs with a -0 addend: no
+          // later step can fuse them, and dl / dh need that dp
           const uint32_t kwk = lds_u32(reinterpret_cast<const uint32_t*>(&rb.kv[k][lane]) + c2);
-          const float2 dp = make_float2(__fmul_rn(g2.x, bf16_lo(kwk)), __fmul_rn(g2.y, bf16_hi(kwk)));
+          uint16_t v0, v1;
+          split_bf16x2(kwk, v0, v1);
+          const float2 dp = make_float2(mul_bf16(g0, v0), mul_bf16(g1, v1));
           const float2 dl = sub2_rn(dp, shi2), dh = sub2_rn(dp, slo2);
           const float2 zl = mul2_rn(pk, fma2_rm(abs2(dl), nrho2, dl));
           const float2 zh = mul2_rn(pk, fma2_rp(abs2(dh), rho2, dh));

@@ -182,20 +182,19 @@ fwd_bitwise_kernel(const FwdParams f) {
       for (int k = 0; k < W; ++k) {
         const float2 a = *reinterpret_cast<const float2*>(ape_s + k * tile_cols + 2 * c2);
         const uint32_t w = lds_u32(reinterpret_cast<const uint32_t*>(&rb.sc[k][lane]) + c2);
-        pz[k] = add2_rn(make_float2(bf16_lo(w), bf16_hi(w)), a);
+        uint16_t s0, s1;
+        split_bf16x2(w, s0, s1);
+        pz[k] = make_float2(add_bf16_f32(s0, a.x), add_bf16_f32(s1, a.y));
       }
-      float2 m = pz[0];
-#pragma unroll
-      for (int k = 1; k < W; ++k) m = make_float2(max_nan(m.x, pz[k].x), max_nan(m.y, pz[k].y));
+      auto zx = [&](int k) { return pz[k].x; };
+      auto zy = [&](int k) { return pz[k].y; };
+      const float2 m = make_float2(max_range<0, W>(zx), max_range<0, W>(zy));
       // smallest logit over the valid slots (fminf skips NaN; m carries it)
-      float2 zmin = pz[W - 1];
-#pragma unroll
-      for (int k = (COFF == 2 ? R : 0); k < W - 1; ++k)
-        zmin = make_float2(fminf(zmin.x, pz[k].x), fminf(zmin.y, pz[k].y));
-      if (COFF == 2 && !cur.first) {
-#pragma unroll
-        for (int k = 0; k < R; ++k) zmin = make_float2(fminf(zmin.x, pz[k].x), fminf(zmin.y, pz[k].y));
-      }
+      constexpr int kLoValid = COFF == 2 ? R : 0;  // first slot valid on every row
+      float2 zmin = make_float2(min_range<kLoValid, W>(zx), min_range<kLoValid, W>(zy));
+      if (COFF == 2 && !cur.first)
+        zmin = make_float2(fminf(zmin.x, min_range<0, (COFF == 2 ? R : 1)>(zx)),
+                           fminf(zmin.y, min_range<0, (COFF == 2 ? R : 1)>(zy)));
       const float2 tau = make_float2(__fsub_ru(m.x, zmin.x), __fsub_ru(m.y, zmin.y));
       float2 den = make_float2(0.0f, 0.0f), psd = den;  // den, the sum of its rounded partial sums
 #pragma unroll
