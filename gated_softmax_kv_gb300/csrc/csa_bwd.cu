@@ -123,10 +123,10 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
       for (int k = 0; k < W; ++k) {
         const float4 a = *reinterpret_cast<const float4*>(ape_s + k * tile_cols);
-        pz[k][0] = __fadd_rn(bf16_lo(scv[k].x), a.x);
-        pz[k][1] = __fadd_rn(bf16_hi(scv[k].x), a.y);
-        pz[k][2] = __fadd_rn(bf16_lo(scv[k].y), a.z);
-        pz[k][3] = __fadd_rn(bf16_hi(scv[k].y), a.w);
+        pz[k][0] = add_bf16_f32(bf16_half(scv[k].x, 0), a.x);
+        pz[k][1] = add_bf16_f32(bf16_half(scv[k].x, 1), a.y);
+        pz[k][2] = add_bf16_f32(bf16_half(scv[k].y, 0), a.z);
+        pz[k][3] = add_bf16_f32(bf16_half(scv[k].y, 1), a.w);
       }
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
@@ -156,7 +156,8 @@ bwd_small_kernel(const BwdParams bp) {
           float acc = 0.0f;
 #pragma unroll
           for (int k = 0; k < W; ++k) {
-            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+            // RN(g kv) from the bf16 halves (the product is exact)
+            const float dp = mul_bf16(bf16_half(c2 ? gv.y : gv.x, h), bf16_half(c2 ? kvv[k].y : kvv[k].x, h));
             acc = __fadd_rn(acc, __fmul_rn(dp, pz[k][c]));
           }
           sum[h] = acc;
@@ -169,7 +170,7 @@ bwd_small_kernel(const BwdParams bp) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int c = 2 * c2 + h;
-            const float dp = __fmul_rn(g[h], bf16_at(c2 ? kvv[k].y : kvv[k].x, h));
+            const float dp = mul_bf16(bf16_half(c2 ? gv.y : gv.x, h), bf16_half(c2 ? kvv[k].y : kvv[k].x, h));
             dz[h] = __fmul_rn(pz[k][c], __fsub_rn(dp, sum[h]));
             dk[h] = __fmul_rn(g[h], pz[k][c]);
             dacc[k][c] = __fadd_rn(dacc[k][c], dz[h]);

@@ -91,6 +91,7 @@ struct ColVec<2> {
   static __device__ __forceinline__ void store(uint16_t* p, T v) { __stcs(reinterpret_cast<uint32_t*>(p), v); }
 #endif
   static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(v, c); }
+  static __device__ __forceinline__ uint16_t half(T v, int c) { return bf16_half(v, c); }
   static __device__ __forceinline__ T zero() { return 0u; }
   static __device__ __forceinline__ T ninf() { return kNegInfBf16x2; }
   static __device__ __forceinline__ T pack(const float* x) { return pack_bf16x2(x[0], x[1]); }
@@ -124,6 +125,7 @@ struct ColVec<4> {
 #endif
   static __device__ __forceinline__ void store(uint16_t* p, T v) { st_stream8(p, v); }
   static __device__ __forceinline__ float elem(T v, int c) { return bf16_at(c < 2 ? v.x : v.y, c & 1); }
+  static __device__ __forceinline__ uint16_t half(T v, int c) { return bf16_half(c < 2 ? v.x : v.y, c & 1); }
   static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
   static __device__ __forceinline__ T ninf() { return make_uint2(kNegInfBf16x2, kNegInfBf16x2); }
   static __device__ __forceinline__ T pack(const float* x) {
@@ -257,8 +259,8 @@ bwd_long_kernel(const BwdParams bp) {
         for (int c = 0; c < VC; c += 2) {
           const float2 a = col_ok ? __ldg(reinterpret_cast<const float2*>(ape_t + t * ld + c))
                                   : make_float2(0.0f, 0.0f);
-          const float2 z =
-              add2_rn(make_float2(V::elem(scw[t], c), V::elem(scw[t], c + 1)), a);
+          const float2 z = make_float2(add_bf16_f32(V::half(scw[t], c), a.x),
+                                       add_bf16_f32(V::half(scw[t], c + 1), a.y));
           pz[t][c] = z.x;
           pz[t][c + 1] = z.y;
         }
@@ -285,7 +287,9 @@ bwd_long_kernel(const BwdParams bp) {
           pz[t][c] = e.x;
           pz[t][c + 1] = e.y;
           sum = add2_rn(sum, e);
-          const float2 dp = mul2_rn(g2, make_float2(V::elem(kvw[t], c), V::elem(kvw[t], c + 1)));
+          // dp = RN(g kv) from the bf16 halves (exact products)
+          const float2 dp = make_float2(mul_bf16(V::half(gw, c), V::half(kvw[t], c)),
+                                        mul_bf16(V::half(gw, c + 1), V::half(kvw[t], c + 1)));
           tsum = fma2_rn(dp, e, tsum);
         }
         mloc[c] = m0;
@@ -345,13 +349,13 @@ bwd_long_kernel(const BwdParams bp) {
         float dz[VC], dk[VC];
 #pragma unroll
         for (int c = 0; c < VC; c += 2) {
-          // a two-lane product is never followed by a two-lane add or
-          // subtract (the compiler may fuse such a pair): dp - S stays scalar
+          // dp = RN(g kv) as bf16-input FMAs (no later step can fuse them),
+          // so dp - S runs on the two-lane subtraction
           const float2 g2 = make_float2(g[c], g[c + 1]);
           const float2 pp = mul2_rn(make_float2(pz[t][c], pz[t][c + 1]), make_float2(fy[c], fy[c + 1]));
-          const float2 diff =
-              make_float2(__fsub_rn(__fmul_rn(g[c], V::elem(kvw[t], c)), Sv[c]),
-                          __fsub_rn(__fmul_rn(g[c + 1], V::elem(kvw[t], c + 1)), Sv[c + 1]));
+          const float2 dp = make_float2(mul_bf16(V::half(gw, c), V::half(kvw[t], c)),
+                                        mul_bf16(V::half(gw, c + 1), V::half(kvw[t], c + 1)));
+          const float2 diff = sub2_rn(dp, make_float2(Sv[c], Sv[c + 1]));
           const float2 z = mul2_rn(pp, diff);
           const float2 k = mul2_rn(g2, pp);
           dz[c] = z.x;

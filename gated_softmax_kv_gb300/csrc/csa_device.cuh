@@ -124,6 +124,57 @@ __device__ __forceinline__ float2 softmax_exp_fast2(float2 x) {
   return make_float2(ex2_approx_ftz(t.x), ex2_approx_ftz(t.y));
 }
 
+// ---- bf16 inputs, three-input max / min ------------------------------------
+
+// The two bf16 halves of a word (lower address first) as 16-bit registers.
+__device__ __forceinline__ void split_bf16x2(uint32_t w, uint16_t& lo, uint16_t& hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+__device__ __forceinline__ uint16_t bf16_half(uint32_t w, int h) {
+  uint16_t lo, hi;
+  split_bf16x2(w, lo, hi);
+  return h ? hi : lo;
+}
+// Mixed-precision forms of the sm_100 family, bf16 inputs read as fp32:
+// RN(a + c) and RN(a b + c). A product of two bf16 values is exact in fp32,
+// so with c = -0 the FMA gives RN(a b), signed zeros included.
+__device__ __forceinline__ float add_bf16_f32(uint16_t a, float c) {
+  float d;
+  asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float mul_bf16(uint16_t a, uint16_t b) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(-0.0f));
+  return d;
+}
+// Three-input max propagating NaN (as max_nan) and min skipping it (as fminf).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Max / min of v[lo, hi) (hi - lo >= 1) with the three-input forms.
+template <int LO, int HI, class F>
+__device__ __forceinline__ float max_range(F v) {
+  float m = v(LO);
+#pragma unroll
+  for (int k = LO + 1; k < HI; k += 2) m = (k + 1 < HI) ? max3_nan(m, v(k), v(k + 1)) : max_nan(m, v(k));
+  return m;
+}
+template <int LO, int HI, class F>
+__device__ __forceinline__ float min_range(F v) {
+  float m = v(LO);
+#pragma unroll
+  for (int k = LO + 1; k < HI; k += 2) m = (k + 1 < HI) ? min3(m, v(k), v(k + 1)) : fminf(m, v(k));
+  return m;
+}
+
 // ---- division ---------------------------------------------------------------
 
 // a / b rounded to nearest from y = RN(1/b): q = RN(a*y), then one
