@@ -76,13 +76,16 @@ bwd_small_kernel(const BwdParams bp) {
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
-  // [W][tile_cols]: the APE slice of this column tile, later the dape combine buffer
+  // [W][tile_cols]: the APE slice of this column tile, later the dape combine
+  // buffer; then the segment arrays (seg_smem_bytes)
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
     sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
+  const SegMap sg = stage_segments(p.cu, p.cuc, p.nseq, reinterpret_cast<int32_t*>(sm + W * tile_cols),
+                                   tid, nthr);
   __syncthreads();
   const float* ape_s = sm + tx * kCv;
 
@@ -93,11 +96,11 @@ bwd_small_kernel(const BwdParams bp) {
     for (int c = 0; c < kCv; ++c) dacc[k][c] = 0.0f;
 
   const uint2 zero2 = make_uint2(0u, 0u);
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * TY;
   int hint = 0;
   for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
-    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    const RowInfo ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
     if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
     const int64_t rowoff = ri.base * ld + j0;
     uint16_t* dkv_row = bp.dkv + rowoff;
@@ -304,7 +307,7 @@ cudaError_t plan_small_d(const Problem& p, BwdShape* s) {
   const int tx = ncv <= 128 ? ncv : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kCv;
+  const size_t smem = sizeof(float) * W * tx * kCv + seg_smem_bytes(p.nseq);
   auto kern = bwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);

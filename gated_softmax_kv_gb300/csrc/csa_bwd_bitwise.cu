@@ -117,6 +117,9 @@ bwd_bitwise_kernel(const BwdParams bp) {
     for (int c2 = 0; c2 < kCv / 2; ++c2) dacc[k][c2] = make_float2(0.0f, 0.0f);
 
   const uint2 zero2 = make_uint2(0u, 0u);
+  // the segment arrays stay in global memory here: a row looks up the row
+  // after it a full row ahead of its use, and the registers of a shared
+  // copy's pointers are what this kernel lacks
   const int64_t true_rows = __ldg(p.cuc + p.nseq);
   const int64_t stride = (int64_t)gridDim.y * TY;
   const uint32_t lt = (1u << lane) - 1u;
@@ -144,16 +147,16 @@ bwd_bitwise_kernel(const BwdParams bp) {
 
   // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
   int64_t b = (int64_t)blockIdx.y * TY + ty;
-  if (b < true_rows) fetch(b, row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
+  if (b < true_rows) fetch(b, row_info_from<true>(p.cu, p.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
   cp_async_commit();
   for (int it = 0; b < true_rows; ++it, b += stride) {
     // the row's map (rows are visited in increasing order, so the segment
     // hint makes this one cached load), then the next row into the other
     // buffer, last read by the previous row
-    const RowInfo cur = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    const RowInfo cur = row_info_from<true>(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
     __syncwarp();
     if (b + stride < true_rows)
-      fetch(b + stride, row_info_from(p.cu, p.cuc, p.nseq, b + stride, true_rows, R, hint),
+      fetch(b + stride, row_info_from<true>(p.cu, p.cuc, p.nseq, b + stride, true_rows, R, hint),
             rbs[(it + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();  // this row's copies have landed ...

@@ -197,7 +197,8 @@ bwd_long_kernel(const BwdParams bp) {
 
   __shared__ float m_s[NCH * LDS], d_s[NCH * LDS], s_s[NCH * LDS];
   __shared__ float M_s[TC], D_s[TC], S_s[TC];
-  // dape sums of the tile, [W][TC]; each cell belongs to one thread
+  // dape sums of the tile, [W][TC] (each cell belongs to one thread), then
+  // the segment arrays (seg_smem_bytes)
   extern __shared__ __align__(16) float dacc_s[];
   float* dacc_t = dacc_s + k0 * TC + lane * VC;  // 8 (VC 2) or 16 (VC 4) byte aligned
 #pragma unroll
@@ -235,12 +236,16 @@ bwd_long_kernel(const BwdParams bp) {
     gb = col_ok ? V::load(bp.grad_out + rb * d + j0) : V::zero();
   };
 
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  // the segment arrays after the dape table, in shared memory when they fit
+  const SegMap sg = stage_segments(p.cu, p.cuc, p.nseq, reinterpret_cast<int32_t*>(dacc_s + W * TC),
+                                   tid, NT);
+  __syncthreads();
+  const int64_t true_rows = sg.cuc[p.nseq];
   int64_t b = blockIdx.y;
   RowInfo ri{};
   int hint = 0;  // segment of the last row looked up (rows only increase)
   if (b < true_rows) {
-    ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
     loads(b, ri, kvw, gw);
   }
   for (; b < true_rows;) {
@@ -307,7 +312,7 @@ bwd_long_kernel(const BwdParams bp) {
     RowInfo rn{};
     typename V::T kvn[KPT], gn = V::zero();
     if (bn < true_rows) {
-      rn = row_info_from(p.cu, p.cuc, p.nseq, bn, true_rows, R, hint);
+      rn = row_info_from(sg.cu, sg.cuc, p.nseq, bn, true_rows, R, hint);
       loads(bn, rn, kvn, gn);
     }
     if (compute) {
@@ -433,8 +438,11 @@ cudaError_t plan_long_d(const Problem& p, BwdShape* s) {
   const int ncv = p.d / LongShape<W>::kVc;
   const int tiles = (ncv + 31) / 32;
   auto kern = bwd_long_kernel<R, COFF, D>;
-  constexpr size_t smem = sizeof(float) * W * 32 * LongShape<W>::kVc;  // dape sums of the tile
-  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem)) return e;
+  // dape sums of the tile, then the segment arrays
+  const size_t smem = sizeof(float) * W * 32 * LongShape<W>::kVc + seg_smem_bytes(p.nseq);
+  // the attribute is set once per kernel: the largest size any problem needs
+  constexpr size_t smem_max = sizeof(float) * W * 32 * LongShape<W>::kVc + kSegSmemBytesMax;
+  if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem_max)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), NT, smem);
   int64_t gy = (int64_t)kGroupingSms * occ / tiles;
   if (gy > p.C) gy = p.C;

@@ -254,17 +254,52 @@ struct RowInfo {
   bool last;         // last block of its segment
 };
 
+// The segment arrays as a kernel reads them: a CTA's copy in shared memory
+// when each has at most kSegSmemMax entries, else the caller's global arrays.
+// A row's lookup (below) then costs shared-memory reads instead of dependent
+// L2 or DRAM loads ahead of the row's own loads; the copy is one round trip in
+// the prologue, next to the APE slice.
+constexpr int kSegSmemMax = 1024;
+__host__ __device__ inline size_t seg_smem_stride(int nseq) {  // entries, 16-byte multiple
+  return ((size_t)(nseq + 1) + 3) / 4 * 4;
+}
+__host__ __device__ inline size_t seg_smem_bytes(int nseq) {
+  return nseq + 1 <= kSegSmemMax ? 2 * sizeof(int32_t) * seg_smem_stride(nseq) : 0;
+}
+constexpr size_t kSegSmemBytesMax = 2 * sizeof(int32_t) * kSegSmemMax;  // seg_smem_bytes' bound
+struct SegMap {
+  const int32_t* cu;   // cu_seqlens[0 .. nseq]
+  const int32_t* cuc;  // cu_seqlens_comp[0 .. nseq]
+};
+// Copies the arrays into s (seg_smem_bytes(nseq) bytes, 16-byte aligned) when
+// they fit; the copy is readable after the caller's next __syncthreads.
+__device__ __forceinline__ SegMap stage_segments(const int32_t* cu, const int32_t* cuc, int nseq,
+                                                 int32_t* s, int tid, int nthr) {
+  const int n = nseq + 1;
+  if (n > kSegSmemMax) return SegMap{cu, cuc};
+  const int stride = (int)seg_smem_stride(nseq);
+  for (int i = tid; i < n; i += nthr) {
+    s[i] = __ldg(cu + i);
+    s[stride + i] = __ldg(cuc + i);
+  }
+  return SegMap{s, s + stride};
+}
+
 // Row b < true_rows: s = last segment with cu_seqlens_comp[s] <= b,
 // i = b - cu_seqlens_comp[s], base = cu_seqlens[s] + i * ratio.
 // Row b >= true_rows (static-capacity padding): first block from token 0.
 // For a thread that visits rows in increasing order: `hint` is a segment with
 // cu_seqlens_comp[hint] <= b from an earlier row (0 at first); the common case
 // costs one load, otherwise a binary search over the later segments, which
-// terminates and stays in [0, num_seqs) whatever the arrays hold.
-__device__ __forceinline__ RowInfo row_info_from(const int32_t* __restrict__ cu,
-                                                 const int32_t* __restrict__ cuc, int nseq,
+// terminates and stays in [0, num_seqs) whatever the arrays hold. cu and cuc
+// are generic pointers (a SegMap's shared-memory copy or the global arrays);
+// with kGlobalRO they must be the global arrays, read through the read-only
+// path (loads the compiler may hoist past the kernel's own stores).
+template <bool kGlobalRO = false>
+__device__ __forceinline__ RowInfo row_info_from(const int32_t* cu, const int32_t* cuc, int nseq,
                                                  int64_t b, int64_t true_rows, int ratio,
                                                  int& hint) {
+  auto ld = [](const int32_t* q) -> int32_t { return kGlobalRO ? __ldg(q) : *q; };
   RowInfo ri;
   if (b >= true_rows) {
     ri.base = 0;
@@ -274,21 +309,21 @@ __device__ __forceinline__ RowInfo row_info_from(const int32_t* __restrict__ cu,
     return ri;
   }
   int lo = hint;
-  int64_t c1 = __ldg(cuc + lo + 1);
+  int64_t c1 = ld(cuc + lo + 1);
   if (c1 <= b) {
     int hi = nseq;
     lo = lo + 1;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if ((int64_t)__ldg(cuc + mid) <= b) lo = mid; else hi = mid;
+      if ((int64_t)ld(cuc + mid) <= b) lo = mid; else hi = mid;
     }
-    c1 = __ldg(cuc + lo + 1);
+    c1 = ld(cuc + lo + 1);
   }
   hint = lo;
-  const int64_t c0 = __ldg(cuc + lo);
+  const int64_t c0 = ld(cuc + lo);
   const int64_t i = b - c0;
-  ri.base = (int64_t)__ldg(cu + lo) + i * ratio;
-  ri.seg_end = __ldg(cu + lo + 1);
+  ri.base = (int64_t)ld(cu + lo) + i * ratio;
+  ri.seg_end = ld(cu + lo + 1);
   ri.first = (i == 0);
   ri.last = (i == c1 - c0 - 1);
   return ri;

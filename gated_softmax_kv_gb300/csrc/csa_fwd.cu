@@ -118,22 +118,26 @@ fwd_small_kernel(const FwdParams f) {
   // element offset of slot k from (row base token, column j0)
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
-  // APE slice of this column tile, [W][tile_cols], read once per CTA
+  // APE slice of this column tile, [W][tile_cols], read once per CTA, then
+  // the segment arrays (seg_smem_bytes)
   extern __shared__ float sm[];
   for (int i = tid; i < W * tile_cols; i += nthr) {
     const int k = i / tile_cols;
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
     sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
+  // then the segment arrays
+  const SegMap sg = stage_segments(p.cu, p.cuc, p.nseq, reinterpret_cast<int32_t*>(sm + W * tile_cols),
+                                   tid, nthr);
   __syncthreads();
   if (jv >= nvec) return;  // no barrier below
   const float* ape_s = sm + tx * kVec;
 
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * TY;
   int hint = 0;
   for (int64_t b = (int64_t)blockIdx.y * TY + ty; b < p.C; b += stride) {
-    const RowInfo ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    const RowInfo ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
     uint16_t* dst = f.out + b * d + j0;
     if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
       st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
@@ -164,7 +168,7 @@ cudaError_t launch_small_d(const FwdParams& f, cudaStream_t stream) {
   const int tx = nvec <= 128 ? nvec : 128;
   const int ty = kThreads / tx > 0 ? kThreads / tx : 1;
   const int tiles = (nvec + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kVec;
+  const size_t smem = sizeof(float) * W * tx * kVec + seg_smem_bytes(f.p.nseq);
   auto kern = fwd_small_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);

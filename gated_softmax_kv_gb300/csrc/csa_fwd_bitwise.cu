@@ -78,7 +78,8 @@ fwd_bitwise_kernel(const FwdParams f) {
   auto koff = [&](int k) -> int64_t { return (S::tok(0, k)) * ld + S::half(k) * d; };
 
   // [W][tile_cols] APE slice, then two row buffers per warp (the current row
-  // and the next one, in flight), then the warps' queues of undecided columns
+  // and the next one, in flight), then the warps' queues of undecided
+  // columns, then the segment arrays (seg_smem_bytes)
   extern __shared__ float sm[];
   __shared__ float tab[2 * kExpTableSize];
   exp_cr_table(tab);
@@ -87,16 +88,19 @@ fwd_bitwise_kernel(const FwdParams f) {
     const int col = blockIdx.x * tile_cols + (i - k * tile_cols);
     sm[i] = col < d ? __ldg(p.ape + (int64_t)S::ape_row(k) * ld + S::half(k) * d + col) : 0.0f;
   }
-  __syncthreads();
-  const float* ape_s = sm + tx * kCv;
   RowBuf<W>* const rb0 = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols);
   RowBuf<W>* rbs = rb0 + 2 * (tid >> 5);
-  Pending<W>& pq = reinterpret_cast<Pending<W>*>(rb0 + 2 * (nthr >> 5))[tid >> 5];
+  Pending<W>* const pq0 = reinterpret_cast<Pending<W>*>(rb0 + 2 * (nthr >> 5));
+  Pending<W>& pq = pq0[tid >> 5];
+  const SegMap sg = stage_segments(p.cu, p.cuc, p.nseq, reinterpret_cast<int32_t*>(pq0 + (nthr >> 5)),
+                                   tid, nthr);
+  __syncthreads();
+  const float* ape_s = sm + tx * kCv;
   constexpr int kCap = Pending<W>::kCap;
   static_assert(kCap == P, "a pass takes the whole queue");
 
   const uint2 zero2 = make_uint2(0u, 0u);
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * TY;
   const uint32_t lt = (1u << lane) - 1u;
   int hint = 0;
@@ -156,13 +160,13 @@ fwd_bitwise_kernel(const FwdParams f) {
 
   // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
   int64_t b = (int64_t)blockIdx.y * TY + ty;
-  if (b < p.C) fetch(row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
+  if (b < p.C) fetch(row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint), rbs[0]);
   cp_async_commit();
   for (int it = 0; b < p.C; ++it, b += stride) {
-    const RowInfo cur = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+    const RowInfo cur = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
     __syncwarp();
     if (b + stride < p.C)
-      fetch(row_info_from(p.cu, p.cuc, p.nseq, b + stride, true_rows, R, hint), rbs[(it + 1) & 1]);
+      fetch(row_info_from(sg.cu, sg.cuc, p.nseq, b + stride, true_rows, R, hint), rbs[(it + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();  // this row's copies have landed ...
     __syncwarp();        // ... for every lane of the warp
@@ -279,7 +283,8 @@ cudaError_t launch_bitwise_d(const FwdParams& f, cudaStream_t stream) {
   const int ty = kThreads / tx;
   const int tiles = (ncv + tx - 1) / tx;
   const size_t smem = sizeof(float) * W * tx * kCv +
-                      (2 * sizeof(RowBuf<W>) + sizeof(Pending<W>)) * (size_t)(tx * ty / 32);
+                      (2 * sizeof(RowBuf<W>) + sizeof(Pending<W>)) * (size_t)(tx * ty / 32) +
+                      seg_smem_bytes(f.p.nseq);
   auto kern = fwd_bitwise_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);

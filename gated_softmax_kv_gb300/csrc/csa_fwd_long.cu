@@ -73,7 +73,12 @@ fwd_long_kernel(const FwdParams f, const int split) {
   const int nbc = NB / split;  // batches per chunk
   const int jb = chunk * nbc, je = jb + nbc;
 
-  const int64_t true_rows = __ldg(p.cuc + p.nseq);
+  // the segment arrays in shared memory when they fit (seg_smem_bytes)
+  extern __shared__ __align__(16) int32_t seg_s[];
+  const SegMap sg = stage_segments(p.cu, p.cuc, p.nseq, seg_s, threadIdx.y * 32 + threadIdx.x,
+                                   32 * kLongRows);
+  __syncthreads();
+  const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * rows_per_cta;
   int hint = 0;
   int parity = 0;
@@ -83,7 +88,7 @@ fwd_long_kernel(const FwdParams f, const int split) {
     RowInfo ri{};
     bool ok = false;
     if (active) {
-      ri = row_info_from(p.cu, p.cuc, p.nseq, b, true_rows, R, hint);
+      ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
       ok = row_in_bounds<R, COFF>(ri, p.T);
     }
     float m[4], den[4], acc[4];
@@ -225,7 +230,8 @@ cudaError_t launch_long(const FwdParams& f, cudaStream_t stream) {
   auto kern = f.p.d == 512 ? fwd_long_kernel<R, COFF, 512>
              : f.p.d == 128 ? fwd_long_kernel<R, COFF, 128> : fwd_long_kernel<R, COFF, 0>;
   const int rows_per_cta = kLongRows / split;
-  const int occ = occupancy(reinterpret_cast<const void*>(kern), 32 * kLongRows, 0);
+  const size_t smem = seg_smem_bytes(f.p.nseq);
+  const int occ = occupancy(reinterpret_cast<const void*>(kern), 32 * kLongRows, smem);
   const int64_t row_blocks = (f.p.C + rows_per_cta - 1) / rows_per_cta;
   int64_t gy = (int64_t)sm_count() * occ / tiles;
   if (gy < 1) gy = 1;
@@ -234,7 +240,7 @@ cudaError_t launch_long(const FwdParams& f, cudaStream_t stream) {
   const int64_t passes = (row_blocks + gy - 1) / gy;
   gy = (row_blocks + passes - 1) / passes;
   if (gy > 65535) gy = 65535;
-  return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(32, kLongRows), 0, stream, f, split);
+  return launch_dependent(kern, dim3(tiles, (unsigned)gy), dim3(32, kLongRows), smem, stream, f, split);
 }
 
 }  // namespace
