@@ -45,6 +45,14 @@ constexpr int kThreads = 256;
 #ifndef CSA_BWD_SMALL_EXP
 #define CSA_BWD_SMALL_EXP softmax_exp_fast
 #endif
+// 1: windows of up to 4 slots load the next row's inputs before computing the
+// current row (0: one row at a time). Measured at ratio 2, coff 2, d 128
+// (62766 ragged tokens): 33.4 us against 36.5 us with L2 clean, 38.6 against
+// 41.2 us after a write flush.
+#ifndef CSA_BWD_PREFETCH
+#define CSA_BWD_PREFETCH 1
+#endif
+constexpr bool kBwdPrefetch = CSA_BWD_PREFETCH != 0;
 #ifndef CSA_BWD_SMALL_DIV_RN
 #define CSA_BWD_SMALL_DIV_RN 0
 #endif
@@ -99,27 +107,30 @@ bwd_small_kernel(const BwdParams bp) {
   const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * TY;
   int hint = 0;
-  for (int64_t b = (int64_t)blockIdx.y * TY + ty; col_ok && b < true_rows; b += stride) {
-    const RowInfo ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
-    if (!row_in_bounds<R, COFF>(ri, p.T)) continue;  // violated preconditions: skip
+  // row b's inputs (a row that breaks the preconditions, or past capacity,
+  // reads nothing)
+  auto load_row = [&](int64_t b, const RowInfo& ri, uint2 (&kvv)[W], uint2 (&scv)[W], uint2& gv) {
+    if (!row_in_bounds<R, COFF>(ri, p.T) || b >= p.C) return;
+    const int64_t rowoff = ri.base * ld + j0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      if (S::masked(ri.first, k)) {
+        kvv[k] = zero2;
+        scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
+      } else {
+        kvv[k] = ld_stream8(p.kv + rowoff + koff(k));
+        scv[k] = ld_stream8(p.score + rowoff + koff(k));
+      }
+    }
+    gv = ld_stream8(bp.grad_out + b * d + j0);
+  };
+  // row b from its loaded inputs: outputs, dape sums, owned zero positions
+  auto run_row = [&](int64_t b, const RowInfo& ri, uint2 (&kvv)[W], uint2 (&scv)[W], const uint2 gv) {
+    if (!row_in_bounds<R, COFF>(ri, p.T)) return;  // violated preconditions: skip
     const int64_t rowoff = ri.base * ld + j0;
     uint16_t* dkv_row = bp.dkv + rowoff;
     uint16_t* dsc_row = bp.dscore + rowoff;
     if (b < p.C) {
-      const uint16_t* kv_row = p.kv + rowoff;
-      const uint16_t* sc_row = p.score + rowoff;
-      uint2 kvv[W], scv[W];
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        if (S::masked(ri.first, k)) {
-          kvv[k] = zero2;
-          scv[k] = make_uint2(kNegInfBf16x2, kNegInfBf16x2);
-        } else {
-          kvv[k] = ld_stream8(kv_row + koff(k));
-          scv[k] = ld_stream8(sc_row + koff(k));
-        }
-      }
-      const uint2 gv = ld_stream8(bp.grad_out + b * d + j0);
 
       // z = score + ape, then in place e = exp(z - m), then p = e * (1 / den)
       float pz[W][kCv];
@@ -221,6 +232,40 @@ bwd_small_kernel(const BwdParams bp) {
           st_stream8(bp.dscore + off, zero2);
         }
       }
+    }
+  };
+  int64_t b = (int64_t)blockIdx.y * TY + ty;
+  if constexpr (kBwdPrefetch && W <= 4) {
+    // windows of up to 4 slots have the registers for the next row's inputs:
+    // their loads are in flight while this row computes
+    RowInfo ri{};
+    uint2 kvv[W], scv[W], gv = zero2;
+    if (col_ok && b < true_rows) {
+      ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
+      load_row(b, ri, kvv, scv, gv);
+    }
+    for (; col_ok && b < true_rows; b += stride) {
+      RowInfo rn{};
+      uint2 kvn[W], scn[W], gn = zero2;
+      if (b + stride < true_rows) {
+        rn = row_info_from(sg.cu, sg.cuc, p.nseq, b + stride, true_rows, R, hint);
+        load_row(b + stride, rn, kvn, scn, gn);
+      }
+      run_row(b, ri, kvv, scv, gv);
+      ri = rn;
+      gv = gn;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        kvv[k] = kvn[k];
+        scv[k] = scn[k];
+      }
+    }
+  } else {
+    for (; col_ok && b < true_rows; b += stride) {
+      const RowInfo ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
+      uint2 kvv[W], scv[W], gv = zero2;
+      load_row(b, ri, kvv, scv, gv);
+      run_row(b, ri, kvv, scv, gv);
     }
   }
 

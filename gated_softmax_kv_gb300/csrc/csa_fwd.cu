@@ -53,6 +53,14 @@ constexpr int kThreads = 256;
 #ifndef CSA_FWD_EXP2
 #define CSA_FWD_EXP2(x) softmax_exp_fast2(x)
 #endif
+// 1: windows of up to 4 slots load the next row's window before computing the
+// current one; 0 (default): one row at a time. Measured at ratio 2, coff 2,
+// d 128 (62766 ragged tokens, L2 clean): 22.4 us with the prefetch against
+// 21.3 us without, while the backward's prefetch gains 9% on that workload.
+#ifndef CSA_FWD_PREFETCH
+#define CSA_FWD_PREFETCH 0
+#endif
+constexpr bool kFwdPrefetch = CSA_FWD_PREFETCH != 0;
 
 // One output row's 8 columns from the window's kv / score vectors (masked
 // slots already kv = 0, score = -inf) and the APE slice: logits z = score +
@@ -136,28 +144,51 @@ fwd_small_kernel(const FwdParams f) {
   const int64_t true_rows = sg.cuc[p.nseq];
   const int64_t stride = (int64_t)gridDim.y * TY;
   int hint = 0;
-  for (int64_t b = (int64_t)blockIdx.y * TY + ty; b < p.C; b += stride) {
+  // row b's window into kvv / scv (masked slots: kv = 0, score = -inf);
+  // false, and nothing read, for a row that breaks the preconditions
+  auto load_row = [&](int64_t b, uint4 (&kvv)[W], uint4 (&scv)[W]) -> bool {
     const RowInfo ri = row_info_from(sg.cu, sg.cuc, p.nseq, b, true_rows, R, hint);
-    uint16_t* dst = f.out + b * d + j0;
-    if (!row_in_bounds<R, COFF>(ri, p.T)) {  // violated preconditions: NaN, no access
-      st_stream(dst, make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u));
-      continue;
-    }
+    if (!row_in_bounds<R, COFF>(ri, p.T)) return false;
     const int64_t rowoff = ri.base * ld + j0;
-    const uint16_t* kv_row = p.kv + rowoff;
-    const uint16_t* sc_row = p.score + rowoff;
-    uint4 kvv[W], scv[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-      if (S::masked(ri.first, k)) {  // kv = 0, score = -inf
+      if (S::masked(ri.first, k)) {
         kvv[k] = make_uint4(0u, 0u, 0u, 0u);
         scv[k] = make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
       } else {
-        kvv[k] = ld_stream(kv_row + koff(k));
-        scv[k] = ld_stream(sc_row + koff(k));
+        kvv[k] = ld_stream(p.kv + rowoff + koff(k));
+        scv[k] = ld_stream(p.score + rowoff + koff(k));
       }
     }
-    st_stream(dst, small_row_out<W>(kvv, scv, ape_s, tile_cols));
+    return true;
+  };
+  const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+  int64_t b = (int64_t)blockIdx.y * TY + ty;
+  if constexpr (kFwdPrefetch && W <= 4) {
+    // windows of up to 4 slots have the registers for the next row's window:
+    // its loads are in flight while this row computes
+    uint4 kvv[W], scv[W];
+    bool ok = b < p.C && load_row(b, kvv, scv);
+    for (; b < p.C; b += stride) {
+      uint4 kvn[W], scn[W];
+      const bool okn = b + stride < p.C && load_row(b + stride, kvn, scn);
+      st_stream(f.out + b * d + j0, ok ? small_row_out<W>(kvv, scv, ape_s, tile_cols) : nan4);
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        kvv[k] = kvn[k];
+        scv[k] = scn[k];
+      }
+      ok = okn;
+    }
+  } else {
+    for (; b < p.C; b += stride) {
+      uint4 kvv[W], scv[W];
+      if (!load_row(b, kvv, scv)) {  // violated preconditions: NaN, no access
+        st_stream(f.out + b * d + j0, nan4);
+        continue;
+      }
+      st_stream(f.out + b * d + j0, small_row_out<W>(kvv, scv, ape_s, tile_cols));
+    }
   }
 }
 
