@@ -754,9 +754,10 @@ def run_gpu(args, rank, world, local):
                                    "~8 TB/s nominal HBM3e peak, the figure the >= 70% target is "
                                    "stated in"),
                      **traffic, "algorithmic_bytes": dom_bytes, "peak_source": peak_src,
-                     **({"note": "the exact mode is bound by instruction issue and the FMA pipe "
-                                 "(correctly rounded exp), not by HBM; the HBM fraction is shown "
-                                 "for comparison with the default mode"} if args.exact else {})},
+                     **({"note": "the exact mode is bound by instruction issue (the fast "
+                                 "arithmetic plus its error enclosures, and the exact pass over "
+                                 "undecided outputs), not by HBM; the HBM fraction is shown for "
+                                 "comparison with the default mode"} if args.exact else {})},
         "fwd": {"ms": fwd_avg * 1e3, "tokens_per_s": T / fwd_avg, "GBps": fwd_gbs, "frac": fwd_gbs / peak,
                 "frac_of_nominal": fwd_gbs / NOMINAL_HBM_GBS, "algorithmic_bytes": fwd_bytes},
         "bwd": {"ms": bwd_avg * 1e3, "tokens_per_s": T / bwd_avg, "GBps": bwd_gbs, "frac": bwd_gbs / peak,
