@@ -40,6 +40,10 @@ struct Bounds {
 __device__ __forceinline__ void st_u16(uint16_t* p, uint16_t v) {
   asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(v) : "memory");
 }
+// a 4-byte output store (two bf16 columns) that skips L1 allocation
+__device__ __forceinline__ void st_u32_na(uint16_t* p, uint32_t v) {
+  asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint16_t bf16_bits_rn(float x) {
   return (uint16_t)(pack_bf16x2(x, 0.0f) & 0xFFFFu);
 }

@@ -168,7 +168,7 @@ bwd_bitwise_kernel(const BwdParams bp) {
     uint16_t* dsc_row = bp.dscore + rowoff;
     if (b < p.C) {
       // per column pair (the two lanes of f32x2 values): z = score + ape,
-      // then in place e, then p; then the packed bf16 outputs
+      // then in place e, then p; then the pair's bf16 outputs
       float2 pz[W][2];
       int n = 0;  // failing columns of the row so far
 #pragma unroll
@@ -254,8 +254,12 @@ bwd_bitwise_kernel(const BwdParams bp) {
           if (!S::masked(cur.first, k))
             diff |= (wka ^ pack_bf16x2(dkb.x, dkb.y)) | (wzl ^ pack_bf16x2(zh.x, zh.y));
           dacc[k][c2] = add2_rn(dacc[k][c2], add2_rn(zl, zh));
-          // dkv and dscore words of columns 2 c2 and 2 c2 + 1
-          pz[k][c2] = make_float2(__uint_as_float(wka), __uint_as_float(wzl));
+          // dkv and dscore words of columns 2 c2 and 2 c2 + 1, stored now: holding
+          // them for 8-byte stores after the second pair spilled
+          if (col_ok && !S::masked(cur.first, k)) {
+            st_u32_na(dkv_row + koff(k) + 2 * c2, wka);
+            st_u32_na(dsc_row + koff(k) + 2 * c2, wzl);
+          }
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -263,14 +267,6 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const uint32_t mc = __ballot_sync(0xffffffffu, fail);
           if (fail) rb.fail[n + __popc(mc & lt)] = (uint8_t)(lane * kCv + 2 * c2 + h);
           n += __popc(mc);
-        }
-      }
-      if (col_ok) {
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          if (S::masked(cur.first, k)) continue;
-          st_stream8(dkv_row + koff(k), make_uint2(__float_as_uint(pz[k][0].x), __float_as_uint(pz[k][1].x)));
-          st_stream8(dsc_row + koff(k), make_uint2(__float_as_uint(pz[k][0].y), __float_as_uint(pz[k][1].y)));
         }
       }
 
