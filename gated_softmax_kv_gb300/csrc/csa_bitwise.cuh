@@ -113,11 +113,12 @@ struct RowBuf {
   uint8_t fail[32 * kCv];
 };
 
-// A warp's undecided forward outputs waiting for the exact pass, copied out
-// of the row buffers so that a pass takes a full set of 64 / W columns (W / 2
-// lanes a column) whatever rows they came from: each column's window (masked
-// slots as copied in: score -inf, kv 0), its output offset and its column in
-// the block's APE tile.
+// A warp's undecided columns waiting for the exact pass, copied out of the
+// row buffers so that a pass takes a full set of 64 / W columns (W / 2 lanes
+// a column) whatever rows they came from: each column's window (masked slots
+// as copied in: score -inf, kv 0), its output offset, its column in the
+// block's APE tile and, for the backward, grad_out and the row's
+// first-in-segment flag.
 template <int W>
 struct Pending {
   static constexpr int kCap = 64 / W;
@@ -125,6 +126,8 @@ struct Pending {
   uint16_t sc[kCap][W];
   uint16_t kv[kCap][W];
   uint16_t tcol[kCap];
+  uint16_t g[kCap];
+  uint8_t first[kCap];
 };
 
 }  // namespace bitwise

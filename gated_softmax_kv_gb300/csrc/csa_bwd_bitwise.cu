@@ -49,7 +49,10 @@
 //     correctly rounded exp, correctly rounded division, the reference's
 //     slot-order den and S summed by every lane of the column from gathered
 //     values), eight columns per pass at W = 8, and the exact bf16 values
-//     overwrite the fast ones while those lines are still in L2.
+//     overwrite the fast ones while those lines are still in L2. Windows of
+//     up to 4 slots (16- or 32-column passes, about 2 failing columns a
+//     row) copy their failing columns into a per-warp queue instead, and a
+//     full queue, or at the end what is left in it, takes one pass.
 // dape sums the midpoints of the dz enclosures (deterministically, in the
 // two fixed-order levels of the default backward); zero writes and row
 // groups are those of the default small-window backward.
@@ -108,7 +111,14 @@ bwd_bitwise_kernel(const BwdParams bp) {
   }
   __syncthreads();
   const float* ape_s = sm + tx * kCv;
-  RowBuf<W>* rbs = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols) + 2 * (tid >> 5);
+  RowBuf<W>* const rb0 = reinterpret_cast<RowBuf<W>*>(sm + W * tile_cols);
+  RowBuf<W>* rbs = rb0 + 2 * (tid >> 5);
+  // windows of up to 4 slots queue their undecided columns (few per row for
+  // passes of 16 or 32 columns); W = 8 runs one pass per row with failures
+  constexpr bool kQueue = W <= 4;
+  Pending<W>& pq = reinterpret_cast<Pending<W>*>(rb0 + 2 * (nthr >> 5))[tid >> 5];
+  constexpr int kCap = Pending<W>::kCap;
+  static_assert(kCap == P, "a pass takes the whole queue");
 
   float2 dacc[W][kCv / 2];  // sums of dz_lo + dz_hi (twice dz), per column pair
 #pragma unroll
@@ -144,6 +154,54 @@ bwd_bitwise_kernel(const BwdParams bp) {
     if (col_ok) cp_async8(&buf.g[lane], bp.grad_out + row * d + j0);
     else buf.g[lane] = zero2;
   };
+
+  // The exact pass over the first cnt queued columns: as the per-row pass
+  // below, reading the columns from the queue.
+  auto queued_pass = [&](int cnt) {
+    const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
+    const int k0 = 2 * l, k1 = 2 * l + 1;
+    __syncwarp();
+    const bool act = q < cnt;
+    const int qe = act ? q : 0;
+    const uint32_t sw = lds_u32(&pq.sc[qe][k0]);  // slots k0 and k1
+    const uint32_t kw = lds_u32(&pq.kv[qe][k0]);
+    const float g = __uint_as_float((uint32_t)pq.g[qe] << 16);
+    const int tcol = pq.tcol[qe];
+    const bool first = pq.first[qe];
+    const float2 z = make_float2(__fadd_rn(bf16_lo(sw), sm[k0 * tile_cols + tcol]),
+                                 __fadd_rn(bf16_hi(sw), sm[k1 * tile_cols + tcol]));
+    float mx = max_nan(z.x, z.y);
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float2 ex = exp_cr2(sub2_rn(z, make_float2(mx, mx)), tab);
+    float den = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      den = __fadd_rn(den, __shfl_sync(0xffffffffu, (k & 1) ? ex.y : ex.x, gbase + k / 2));
+    const float yd = __frcp_rn(den);
+    const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
+                              make_float2(yd, yd));
+    const float dp0 = __fmul_rn(g, bf16_lo(kw)), dp1 = __fmul_rn(g, bf16_hi(kw));
+    const float t0 = __fmul_rn(dp0, pw.x), t1 = __fmul_rn(dp1, pw.y);
+    float sfin = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      sfin = __fadd_rn(sfin, __shfl_sync(0xffffffffu, (k & 1) ? t1 : t0, gbase + k / 2));
+    if (act) {
+      uint16_t* dk = bp.dkv + pq.off[qe];
+      uint16_t* dz = bp.dscore + pq.off[qe];
+      if (!S::masked(first, k0)) {
+        st_u16(dk + koff(k0), bf16_bits_rn(__fmul_rn(g, pw.x)));
+        st_u16(dz + koff(k0), bf16_bits_rn(__fmul_rn(pw.x, __fsub_rn(dp0, sfin))));
+      }
+      if (!S::masked(first, k1)) {
+        st_u16(dk + koff(k1), bf16_bits_rn(__fmul_rn(g, pw.y)));
+        st_u16(dz + koff(k1), bf16_bits_rn(__fmul_rn(pw.y, __fsub_rn(dp1, sfin))));
+      }
+    }
+    __syncwarp();
+  };
+  int pend = 0;  // queued columns
 
   // every lane of a warp runs every row of its warp (the exact pass is warp-wide)
   int64_t b = (int64_t)blockIdx.y * TY + ty;
@@ -270,8 +328,35 @@ bwd_bitwise_kernel(const BwdParams bp) {
         }
       }
 
-      // ---- exact pass over the warp's failing columns ----
-      if (n > 0) {
+      if constexpr (kQueue) {
+        // queue the row's undecided columns; a full queue takes one exact pass
+        for (int i = 0; i < n;) {
+          const int take = min(n - i, kCap - pend);
+          __syncwarp();
+          for (int j = lane; j < take * W; j += 32) {
+            const int en = j / W, k = j % W;
+            const int e = rb.fail[i + en];
+            const int lo = e >> 2, c = e & 3;  // owning lane and its column
+            pq.sc[pend + en][k] = reinterpret_cast<const uint16_t*>(&rb.sc[k][lo])[c];
+            pq.kv[pend + en][k] = reinterpret_cast<const uint16_t*>(&rb.kv[k][lo])[c];
+          }
+          if (lane < take) {
+            const int e = rb.fail[i + lane];
+            const int lo = e >> 2, c = e & 3;
+            pq.g[pend + lane] = reinterpret_cast<const uint16_t*>(&rb.g[lo])[c];
+            pq.tcol[pend + lane] = (uint16_t)((tx - lane + lo) * kCv + c);
+            pq.first[pend + lane] = cur.first;
+            pq.off[pend + lane] = rowoff + (lo - lane) * kCv + c;
+          }
+          pend += take;
+          i += take;
+          if (pend == kCap) {
+            queued_pass(kCap);
+            pend = 0;
+          }
+        }
+      } else if (n > 0) {
+        // ---- exact pass over the warp's failing columns of this row ----
         const int q = lane / L, l = lane % L, gbase = lane & ~(L - 1);
         const int k0 = 2 * l, k1 = 2 * l + 1;
         const bool m0 = S::masked(cur.first, k0), m1 = S::masked(cur.first, k1);
@@ -356,6 +441,9 @@ bwd_bitwise_kernel(const BwdParams bp) {
       }
     }
   }
+  if constexpr (kQueue) {
+    if (pend > 0) queued_pass(pend);
+  }
   cp_async_wait<0>();
 
   zero_orphans(bp, R);
@@ -392,7 +480,9 @@ cudaError_t plan_bitwise_d(const Problem& p, BwdShape* s) {
   tx = (tx + 31) / 32 * 32;  // whole warps in a row
   const int ty = kThreads / tx;
   const int tiles = (ncv + tx - 1) / tx;
-  const size_t smem = sizeof(float) * W * tx * kCv + 2 * sizeof(RowBuf<W>) * (size_t)(tx * ty / 32);
+  // the queue of undecided columns at windows of up to 4 slots (the kernel's kQueue)
+  const size_t smem = sizeof(float) * W * tx * kCv +
+                      (2 * sizeof(RowBuf<W>) + (W <= 4 ? sizeof(Pending<W>) : 0)) * (size_t)(tx * ty / 32);
   auto kern = bwd_bitwise_kernel<R, COFF, D>;
   if (cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern), 128 * 1024)) return e;
   const int occ = occupancy(reinterpret_cast<const void*>(kern), tx * ty, smem);
