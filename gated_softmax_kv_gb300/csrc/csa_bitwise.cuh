@@ -25,15 +25,25 @@ constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
 
 template <int W>
 struct Bounds {
-  // rho = (kExpC1 tau + 2 kExpC0 + kExpC1 (W - 1) / e + 4) 2^-24
-  //       + 2^-23 (sum of den's partial sums) / den,
-  // every term widened by 2^-10 (second-order terms, the inversion p / p_ref
-  // -> p_ref / p and the rounding of the partial-sum ratio)
+  // p_ref / p = (1 + delta_k)(1 + Delta), with a slot's own part
+  //   |delta_k| <= rho_own = (kExpC1 tau + kExpC0 + 2.5) 2^-24
+  // (its exp on both sides, its product and quotient roundings) and a part
+  // common to every slot of the column
+  //   |Delta| <= rho_com = (kExpC0 + kExpC1 (W - 1) / e + 1.5) 2^-24
+  //                        + 2^-23 (sum of den's partial sums) / den
+  // (the exps' weighted contribution to den, den's roundings on both sides,
+  // the reciprocal); rho = rho_own + rho_com bounds p_ref / p - 1 as a whole.
+  // Every term is widened by 2^-10 (second-order terms, the inversion
+  // p / p_ref -> p_ref / p and the rounding of the partial-sum ratio).
   static constexpr float kC1u = kExpC1 * kU * 1.0009765625f;
-  static constexpr float kK0u =
-      (2.0f * kExpC0 + kExpC1 * (W - 1) * 0.36787944117144233f + 4.0f) * kU * 1.0009765625f;
+  static constexpr float kKown = (kExpC0 + 2.5f) * kU * 1.0009765625f;
+  static constexpr float kKcom =
+      (kExpC0 + kExpC1 * (W - 1) * 0.36787944117144233f + 1.5f) * kU * 1.0009765625f;
   static constexpr float k2u = 2.0f * kU * 1.0009765625f;
-  // sigma = ((rho + 2^-23) A + 2^-23 (sum of |S's partial sums|)) (1 + 2^-16)
+  // A slot-order sum of RN(x_k p_k) (S, or the pooled sum) then lies within
+  //   sigma = ((rho_own + 2^-23) A + rho_com |sum| + 2^-23 (sum of |its partial sums|)) (1 + 2^-16)
+  // of the reference's, A = sum |terms|: the common factor scales the whole
+  // sum, so it counts against |sum| rather than A
   static constexpr float kWiden = 1.0000152587890625f;
 };
 

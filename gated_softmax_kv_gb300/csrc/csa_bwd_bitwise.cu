@@ -19,15 +19,18 @@
 //     sum of its terms by at most 2^-24 times the sum of its rounded partial
 //     sums, on either side. From these, with tau >= max |t_k| over the
 //     window's valid slots:
-//       p_ref in p [1 - rho, 1 + rho],
-//       rho = (kExpC1 tau + 2 kExpC0 + kExpC1 (W - 1) / e + 4) 2^-24 + 2^-23 P_den / den:
-//     the slot's own exp, the exps' weighted contribution to den (at most
-//     kExpC0 + kExpC1 (W - 1) / e, since t e^t >= -1/e and den >= 1), both
-//     sides' den rounding (P_den = the sum of den's partial sums), the
-//     reciprocal, product and quotient roundings and the inversion of the
-//     ratio; and
+//       p_ref = p (1 + delta_k)(1 + Delta), |delta_k| <= rho_own, |Delta| <= rho_com,
+//       rho_own = (kExpC1 tau + kExpC0 + 2.5) 2^-24,
+//       rho_com = (kExpC0 + kExpC1 (W - 1) / e + 1.5) 2^-24 + 2^-23 P_den / den:
+//     the slot's own exp, product and quotient roundings; and, common to the
+//     column, the exps' weighted contribution to den (at most kExpC0 +
+//     kExpC1 (W - 1) / e, since t e^t >= -1/e and den >= 1), both sides' den
+//     rounding (P_den = the sum of den's partial sums) and the reciprocal
+//     (each bound also covers the inversion of the ratio); so p_ref lies in
+//     p [1 - rho, 1 + rho], rho = rho_own + rho_com; and, since the common
+//     factor scales the whole sum,
 //       S_ref in [S - sigma, S + sigma],
-//       sigma = (rho + 2^-23) A + 2^-23 P_S,
+//       sigma = (rho_own + 2^-23) A + rho_com |S| + 2^-23 P_S,
 //     with A = sum |RN(dp p)| and P_S the sum of |S's partial sums|. Each
 //     enclosure is then pushed through the
 //     reference's own monotone steps with directed rounding:
@@ -279,11 +282,15 @@ bwd_bitwise_kernel(const BwdParams bp) {
           if (k > 0) pss = add2_ru(pss, abs2(acc));
         }
         const float2 k2u = make_float2(B::k2u, B::k2u);
-        const float2 rho2 = fma2_rp(mul2_ru(psd, y), k2u,
-                                    fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kK0u, B::kK0u)));
+        // the weights' own and common relative bounds (Bounds): rho = their
+        // sum for dkv and dz, the common one against |S| in sigma
+        const float2 rown = fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kKown, B::kKown));
+        const float2 rcom = fma2_rp(mul2_ru(psd, y), k2u, make_float2(B::kKcom, B::kKcom));
+        const float2 rho2 = add2_ru(rown, rcom);
         const float2 nrho2 = make_float2(-rho2.x, -rho2.y);
-        const float2 sigma = mul2_ru(fma2_rp(add2_ru(rho2, k2u), aabs, mul2_ru(k2u, pss)),
-                                     make_float2(B::kWiden, B::kWiden));
+        const float2 sigma = mul2_ru(
+            fma2_rp(add2_ru(rown, k2u), aabs, fma2_rp(rcom, abs2(acc), mul2_ru(k2u, pss))),
+            make_float2(B::kWiden, B::kWiden));
         const float2 slo2 = sub2_rd(acc, sigma), shi2 = add2_ru(acc, sigma);
         // g -/+ rho |g| rounded outwards, with the sign of g: the directed
         // roundings give -0 / +0 at g = +0 / -0, and g p_ref has g's sign

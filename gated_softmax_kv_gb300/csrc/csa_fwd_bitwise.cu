@@ -13,11 +13,12 @@
 //     and the reference's pooled sum acc = sum RN(p_k kv_k) in slot order
 //     with those weights;
 //  2. encloses the reference's pooled sum exactly as the bitwise backward
-//     encloses its S (csa_bwd_bitwise.cu): with rho the relative bound of the
-//     weights (softmax_exp_fast's envelope, both sides' den rounding through
-//     the sum of den's partial sums, the quotient roundings),
+//     encloses its S (csa_bwd_bitwise.cu): with rho_own and rho_com the
+//     weights' per-slot and column-common relative bounds (softmax_exp_fast's
+//     envelope, both sides' den rounding through the sum of den's partial
+//     sums, the product and quotient roundings),
 //       acc_ref in [acc - sigma, acc + sigma],
-//       sigma = (rho + 2^-23) A + 2^-23 P,
+//       sigma = (rho_own + 2^-23) A + rho_com |acc| + 2^-23 P,
 //     A = sum |RN(p_k kv_k)|, P = sum of |acc's partial sums| (the kv values
 //     are the reference's own, so each term's only uncertainty is p);
 //  3. accepts bf16(acc) when RD(acc - sigma) and RU(acc + sigma) round to the
@@ -219,10 +220,12 @@ fwd_bitwise_kernel(const FwdParams f) {
         if (k > 0) pss = add2_ru(pss, abs2(acc));
       }
       const float2 k2u = make_float2(B::k2u, B::k2u);
-      const float2 r = fma2_rp(mul2_ru(psd, y), k2u,
-                               fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kK0u, B::kK0u)));
-      const float2 sigma = mul2_ru(fma2_rp(add2_ru(r, k2u), aabs, mul2_ru(k2u, pss)),
-                                   make_float2(B::kWiden, B::kWiden));
+      // the weights' own and common relative bounds (Bounds), then sigma
+      const float2 rown = fma2_rp(tau, make_float2(B::kC1u, B::kC1u), make_float2(B::kKown, B::kKown));
+      const float2 rcom = fma2_rp(mul2_ru(psd, y), k2u, make_float2(B::kKcom, B::kKcom));
+      const float2 sigma = mul2_ru(
+          fma2_rp(add2_ru(rown, k2u), aabs, fma2_rp(rcom, abs2(acc), mul2_ru(k2u, pss))),
+          make_float2(B::kWiden, B::kWiden));
       const float2 lo = sub2_rd(acc, sigma), hi = add2_ru(acc, sigma);
       ow[c2] = pack_bf16x2(lo.x, lo.y);
       const uint32_t diff = ow[c2] ^ pack_bf16x2(hi.x, hi.y);
