@@ -30,9 +30,9 @@
 //     exact pass that overwrites the fast outputs: W / 2 lanes per column,
 //     two window slots a lane (correctly rounded exp, correctly rounded
 //     division, den and the pooled sum in slot order, summed by every lane
-//     of the column from gathered values). About 0.5% of the columns fail
-//     at the headline, so a pass comes every ~12 rows of a warp instead of a
-//     nearly empty one in half the rows.
+//     of the column from gathered values). About 0.3% of the columns fail
+//     at ratio 4, coff 2, head_dim 512, so a pass comes every ~20 rows of a
+//     warp instead of a nearly empty one in a third of the rows.
 // Rows arrive in a per-warp shared-memory buffer by cp.async one row ahead of
 // their computation. A row whose window leaves [0, total_tokens) (violated
 // caller preconditions) gets NaN and reads nothing.
