@@ -53,14 +53,6 @@ constexpr int kThreads = 256;
 #ifndef CSA_FWD_EXP2
 #define CSA_FWD_EXP2(x) softmax_exp_fast2(x)
 #endif
-// 1: windows of up to 4 slots load the next row's window before computing the
-// current one; 0 (default): one row at a time. Measured at ratio 2, coff 2,
-// d 128 (62766 ragged tokens, L2 clean): 22.4 us with the prefetch against
-// 21.3 us without, while the backward's prefetch gains 9% on that workload.
-#ifndef CSA_FWD_PREFETCH
-#define CSA_FWD_PREFETCH 0
-#endif
-constexpr bool kFwdPrefetch = CSA_FWD_PREFETCH != 0;
 
 // One output row's 8 columns from the window's kv / score vectors (masked
 // slots already kv = 0, score = -inf) and the APE slice: logits z = score +
@@ -163,32 +155,16 @@ fwd_small_kernel(const FwdParams f) {
     return true;
   };
   const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-  int64_t b = (int64_t)blockIdx.y * TY + ty;
-  if constexpr (kFwdPrefetch && W <= 4) {
-    // windows of up to 4 slots have the registers for the next row's window:
-    // its loads are in flight while this row computes
+  // one row at a time (a next-row prefetch, which the small backward uses at
+  // windows of up to 4 slots, measured slower here: 22.4 against 21.3 us at
+  // ratio 2, coff 2, d 128, 62766 ragged tokens)
+  for (int64_t b = (int64_t)blockIdx.y * TY + ty; b < p.C; b += stride) {
     uint4 kvv[W], scv[W];
-    bool ok = b < p.C && load_row(b, kvv, scv);
-    for (; b < p.C; b += stride) {
-      uint4 kvn[W], scn[W];
-      const bool okn = b + stride < p.C && load_row(b + stride, kvn, scn);
-      st_stream(f.out + b * d + j0, ok ? small_row_out<W>(kvv, scv, ape_s, tile_cols) : nan4);
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        kvv[k] = kvn[k];
-        scv[k] = scn[k];
-      }
-      ok = okn;
+    if (!load_row(b, kvv, scv)) {  // violated preconditions: NaN, no access
+      st_stream(f.out + b * d + j0, nan4);
+      continue;
     }
-  } else {
-    for (; b < p.C; b += stride) {
-      uint4 kvv[W], scv[W];
-      if (!load_row(b, kvv, scv)) {  // violated preconditions: NaN, no access
-        st_stream(f.out + b * d + j0, nan4);
-        continue;
-      }
-      st_stream(f.out + b * d + j0, small_row_out<W>(kvv, scv, ape_s, tile_cols));
-    }
+    st_stream(f.out + b * d + j0, small_row_out<W>(kvv, scv, ape_s, tile_cols));
   }
 }
 
