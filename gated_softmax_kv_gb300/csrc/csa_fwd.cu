@@ -98,8 +98,11 @@ __device__ __forceinline__ uint4 small_row_out(const uint4 (&kvv)[W], const uint
 
 // D > 0 fixes head_dim at compile time (slot offsets become immediates);
 // D == 0 reads it from the problem.
+// Windows of up to 4 slots fit three CTAs per SM (80 registers): 8-13% faster
+// than two on the ratio-2 and ratio-4 coff-1 workloads (62766 ragged tokens at
+// d 128, 8 x 4096 at d 512, 3 x 8192 at d 128, L2 flushed). W = 8 needs 128.
 template <int R, int COFF, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, (COFF * R <= 4 ? 3 : 2))
 fwd_small_kernel(const FwdParams f) {
   grid_dependency_wait();
   allow_dependent_launch();
