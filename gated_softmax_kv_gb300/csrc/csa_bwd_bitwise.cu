@@ -168,11 +168,15 @@ bwd_bitwise_kernel(const BwdParams bp) {
     const int qe = act ? q : 0;
     const uint32_t sw = lds_u32(&pq.sc[qe][k0]);  // slots k0 and k1
     const uint32_t kw = lds_u32(&pq.kv[qe][k0]);
-    const float g = __uint_as_float((uint32_t)pq.g[qe] << 16);
+    const uint16_t gh = pq.g[qe];
+    const float g = __uint_as_float((uint32_t)gh << 16);
     const int tcol = pq.tcol[qe];
     const bool first = pq.first[qe];
-    const float2 z = make_float2(__fadd_rn(bf16_lo(sw), sm[k0 * tile_cols + tcol]),
-                                 __fadd_rn(bf16_hi(sw), sm[k1 * tile_cols + tcol]));
+    uint16_t s0, s1, v0, v1;
+    split_bf16x2(sw, s0, s1);
+    split_bf16x2(kw, v0, v1);
+    const float2 z = make_float2(add_bf16_f32(s0, sm[k0 * tile_cols + tcol]),
+                                 add_bf16_f32(s1, sm[k1 * tile_cols + tcol]));
     float mx = max_nan(z.x, z.y);
 #pragma unroll
     for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -184,7 +188,7 @@ bwd_bitwise_kernel(const BwdParams bp) {
     const float yd = __frcp_rn(den);
     const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
                               make_float2(yd, yd));
-    const float dp0 = __fmul_rn(g, bf16_lo(kw)), dp1 = __fmul_rn(g, bf16_hi(kw));
+    const float dp0 = mul_bf16(gh, v0), dp1 = mul_bf16(gh, v1);  // RN(g kv), exact
     const float t0 = __fmul_rn(dp0, pw.x), t1 = __fmul_rn(dp1, pw.y);
     float sfin = 0.0f;
 #pragma unroll
@@ -375,15 +379,14 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const uint16_t* kv16 = reinterpret_cast<const uint16_t*>(&rb.kv[0][lo]) + c;
           const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(&rb.sc[0][lo]) + c;
           constexpr int kStride = 32 * 4;  // 16-bit units from one slot's words to the next
-          const float sc0 = m0 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k0 * kStride] << 16);
-          const float sc1 = m1 ? -__int_as_float(0x7f800000) : __uint_as_float((uint32_t)sc16[k1 * kStride] << 16);
-          const float x0 = m0 ? 0.0f : __uint_as_float((uint32_t)kv16[k0 * kStride] << 16);
-          const float x1 = m1 ? 0.0f : __uint_as_float((uint32_t)kv16[k1 * kStride] << 16);
-          const float g =
-              __uint_as_float((uint32_t)(reinterpret_cast<const uint16_t*>(&rb.g[lo])[c]) << 16);
+          // masked slots hold score -inf and kv 0 in the row buffer, as copied in
+          const uint16_t s0 = sc16[k0 * kStride], s1 = sc16[k1 * kStride];
+          const uint16_t v0 = kv16[k0 * kStride], v1 = kv16[k1 * kStride];
+          const uint16_t gh = reinterpret_cast<const uint16_t*>(&rb.g[lo])[c];
+          const float g = __uint_as_float((uint32_t)gh << 16);
           const int tcol = (tx - lane + lo) * kCv + c;
-          const float2 z = make_float2(__fadd_rn(sc0, sm[k0 * tile_cols + tcol]),
-                                       __fadd_rn(sc1, sm[k1 * tile_cols + tcol]));
+          const float2 z = make_float2(add_bf16_f32(s0, sm[k0 * tile_cols + tcol]),
+                                       add_bf16_f32(s1, sm[k1 * tile_cols + tcol]));
           float mx = max_nan(z.x, z.y);
 #pragma unroll
           for (int o = 1; o < L; o <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -397,7 +400,7 @@ bwd_bitwise_kernel(const BwdParams bp) {
           const float yd = __frcp_rn(den);
           const float2 pw = div2_cr(ex, make_float2(den, den), make_float2(-den, -den),
                                     make_float2(yd, yd));
-          const float dp0 = __fmul_rn(g, x0), dp1 = __fmul_rn(g, x1);
+          const float dp0 = mul_bf16(gh, v0), dp1 = mul_bf16(gh, v1);  // RN(g kv), exact
           const float t0 = __fmul_rn(dp0, pw.x), t1 = __fmul_rn(dp1, pw.y);
           float sfin = 0.0f;
 #pragma unroll
