@@ -276,12 +276,9 @@ bwd_long_kernel(const BwdParams bp) {
       // pairs through the two-lane fp32 instructions (same roundings).
 #pragma unroll
       for (int c = 0; c < VC; c += 2) {
-        float m0 = pz[0][c], m1 = pz[0][c + 1];
-#pragma unroll
-        for (int t = 1; t < KPT; ++t) {
-          m0 = max_nan(m0, pz[t][c]);
-          m1 = max_nan(m1, pz[t][c + 1]);
-        }
+        // the chunk's max per column (three-input max, NaN propagating)
+        const float m0 = max_range<0, KPT>([&](int t) { return pz[t][c]; });
+        const float m1 = max_range<0, KPT>([&](int t) { return pz[t][c + 1]; });
         // an all -inf chunk contributes 0
         const float2 mu = make_float2(m0 == kNegInf ? 0.0f : m0, m1 == kNegInf ? 0.0f : m1);
         const float2 g2 = make_float2(g[c], g[c + 1]);
