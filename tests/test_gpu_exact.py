@@ -112,11 +112,15 @@ def test_exact_mode_head_dims(d):
     check_exact(case)
 
 
-def test_exact_mode_wide_logits():
+@pytest.mark.parametrize("ratio,coff", EXACT_SHAPES)
+def test_exact_mode_wide_logits(ratio, coff):
     """Logits spread over a wide range, so that exp arguments reach far below
     zero, underflow to subnormals and to zero: the correctly rounded exp and
-    its fp64 fallback carry the oracle's bits there too."""
-    case = workloads.make_case("exact-wide", [64, 130, 33], 4, 2, 128, pad_rows=1, seed=9)
+    its fp64 fallback carry the oracle's bits there too. Nearly every column
+    fails the enclosure test, so the queues of undecided columns (forward;
+    backward at windows of up to 4 slots) fill several times within a row."""
+    case = workloads.make_case(f"exact-wide-r{ratio}c{coff}", [16 * ratio, 33 * ratio + 3, 8 * ratio + 1],
+                               ratio, coff, 128, pad_rows=1, seed=9)
     rng = np.random.default_rng(9)
     vals = rng.uniform(-120.0, 40.0, size=case.score.shape).astype(np.float32)
     case.score[:] = workloads.f32_to_bf16_bits(vals)
